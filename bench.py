@@ -1,0 +1,475 @@
+"""Benchmark of the ZeRO-3 sharded layer step on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over one layer: forward
+all-gather, backward all-gather, fused reduce-scatter + Adam (three kernel
+launches, one C-ABI call ``z3_step_layer``).  Default workload: one d=1024
+transformer layer (Wqkv, Wo, W_up, W_down, two norm gains; Psi = 12,584,960)
+over N_d = 8 logical ranks, bf16 params/grads, fp32 master/m/v.
+
+Metric: algorithmic HBM bytes of the step ((2 N_d + 34) bytes per unpadded
+element) per second, plus params/s and the fraction of the 8 TB/s HBM
+figure.  Every step works on one of several rotating replicas of the layer
+state whose total is far above the 129 MB L2, so each step starts cold.
+
+Arms:
+  default            the CUDA library (inputs resident in HBM)
+  --impl reference   the plain CPU oracle on the host cores, on a bounded
+                     sample of the same workload (rank 0 only)
+Under torchrun (N > 1) every rank runs an independent replica (weak
+scaling); the timed region is bracketed by a barrier and the max over ranks
+is taken.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sharded ZeRO-3 layer step GB/s and params/s, % of GB300 8 TB/s HBM roofline"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+
+
+# --------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            peaks = json.load(f)
+        return float(peaks["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("z3_kernels.cu", "z3_internal.h"):
+        with open(os.path.join(ROOT, "optimizer_state_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get(kernel, {}).get(workload)
+    if not ent or ent.get("source_digest") != kernel_source_digest():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples taken while the timed region runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            rows.append((t, parts))
+        inside = [r for t, r in rows if self.t0 is not None and self.t0 - 0.06 <= t <= self.t1 + 0.06]
+        use = inside if inside else rows
+        sm = sorted(float(r[1]) for r in use if r[1].replace(".", "").isdigit())
+        mx = [float(r[2]) for r in use if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons,
+                "samples": len(use),
+                "samples_inside_timed_region": len(inside)}
+
+
+# --------------------------------------------------------------------------
+# the CUDA arm
+# --------------------------------------------------------------------------
+
+class Replica:
+    """One copy of the layer state: shards, master, m, v, gradients, and the
+    transient gathered buffer."""
+
+    def __init__(self, z3, L, w, seed, dev):
+        import torch
+        from optimizer_state_gb300 import inputs as I
+        T = L.psi_padded
+        gen = I.make_generator(seed, dev)
+        full = I.draw_master(w, gen, dev)
+        self.shards = torch.empty(T, dtype=torch.bfloat16, device=dev)
+        self.master = torch.empty(T, dtype=torch.float32, device=dev)
+        self.m = torch.empty(T, dtype=torch.float32, device=dev)
+        self.v = torch.empty(T, dtype=torch.float32, device=dev)
+        self.full = torch.empty(L.psi, dtype=torch.bfloat16, device=dev)
+        self.grads = I.draw_grads(w, gen, dev)
+        z3.z3_partition(L, full, self.shards, self.master, self.m, self.v)
+        del full
+        self.step = 0
+
+
+def run_cuda(args, world, rank, local):
+    import torch
+    import torch.distributed as dist
+    from optimizer_state_gb300 import build as libbuild
+    from optimizer_state_gb300 import inputs as I
+    from optimizer_state_gb300 import z3
+
+    libbuild.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = I.LAYER_D1024
+    L = z3.Layout(w.numel, w.n_ranks)
+    stats = L.stats()
+    step_bytes = stats["hbm_step_layer"]
+    scale = 1.0 / w.n_ranks
+    state_bytes = (2 + 4 * 3) * L.psi_padded + 2 * L.psi + 2 * w.n_ranks * w.grad_stride
+    n_rep = max(2, -(-args.cold_bytes // state_bytes))
+    reps = [Replica(z3, L, w, seed=1000 * rank + i, dev=dev) for i in range(n_rep)]
+    stream = torch.cuda.current_stream()
+    sid = stream.cuda_stream
+    launches_per_step = 2 * len_tabs(L, "gather") + len_tabs(L, "reduce")
+
+    def step(rep):
+        rep.step += 1
+        z3.z3_step_layer(L, rep.shards, rep.full, rep.grads, w.grad_stride, scale, rep.master,
+                         rep.m, rep.v, HP, rep.step, stream=sid)
+
+    for i in range(args.warmup):
+        step(reps[i % n_rep])
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    # ---- timed region: K layer steps
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    clocks.mark(True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(reps[i % n_rep])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark(False)
+    if world > 1:
+        dist.barrier()
+    ms_total = e0.elapsed_time(e1)
+    clock_info = clocks.stop()
+
+    # ---- per-kernel timing pass (same launches, events between kernels)
+    kernel_steps = min(args.steps, args.kernel_steps)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(kernel_steps)]
+    torch.cuda.synchronize()
+    for i in range(kernel_steps):
+        rep = reps[i % n_rep]
+        rep.step += 1
+        ev[i][0].record(stream)
+        z3.z3_allgather(L, rep.shards, rep.full, stream=sid)
+        ev[i][1].record(stream)
+        z3.z3_allgather(L, rep.shards, rep.full, stream=sid)
+        ev[i][2].record(stream)
+        z3.z3_reduce_scatter_adam(L, rep.grads, w.grad_stride, scale, None, rep.master, rep.m,
+                                  rep.v, rep.shards, HP, rep.step, stream=sid)
+        ev[i][3].record(stream)
+    torch.cuda.synchronize()
+    t_ag = sum(e[0].elapsed_time(e[1]) + e[1].elapsed_time(e[2]) for e in ev) / (2 * kernel_steps)
+    t_rs = sum(e[2].elapsed_time(e[3]) for e in ev) / kernel_steps
+
+    # ---- end to end through the public API with host buffers
+    e2e = run_e2e(args, z3, L, w, reps[0], stream, sid, step_bytes, world)
+
+    ms_max = ms_total
+    if world > 1:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+    ms_step = ms_max / args.steps
+    value = world * step_bytes * args.steps / (ms_max * 1e-3) / 1e9
+
+    if rank == 0:
+        peak, peak_kind = measured_hbm_peak()
+        rs_bytes = stats["hbm_reduce_scatter_adam"]
+        achieved = rs_bytes / (t_rs * 1e-3) / 1e9
+        traffic = profiled_traffic("k_reduce_rs_adam", "layer_d1024_nd8")
+        line = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_step, 6),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic",
+            "config": {
+                "workload": "layer_d1024_nd8",
+                "layer": "d_model=1024: Wqkv[3072,1024] Wo[1024,1024] W_up[4096,1024] "
+                         "W_down[1024,4096] 2x norm[1024]",
+                "psi": L.psi, "n_ranks": w.n_ranks, "S": L.S,
+                "storage": "bf16 params/grads, fp32 master/m/v",
+                "bytes_per_param": 2 * w.n_ranks + 34,
+                "step_bytes": step_bytes,
+                "l2": f"{n_rep} rotating replicas of the layer state "
+                      f"({n_rep * state_bytes / 1e9:.2f} GB > 129 MB L2), every step cold",
+                "parallelism": f"{world} independent replica(s), one per GPU",
+            },
+            "params_per_s": round(world * L.psi * args.steps / (ms_max * 1e-3), 1),
+            "pct_of_8tbs": round(100.0 * value / (NOMINAL_HBM_GBS * world), 2),
+            "kernels_ms": {"allgather": round(t_ag, 6), "reduce_scatter_adam": round(t_rs, 6)},
+            "roofline": {
+                "kernel": "k_reduce<aligned, RS+Adam> (fused reduce-scatter + Adam)",
+                "bound": "hbm",
+                "achieved": round(achieved, 2),
+                "peak": peak,
+                "peak_kind": peak_kind,
+                "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": traffic,
+                "algorithmic_bytes_per_launch": rs_bytes,
+            },
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clock_info,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def len_tabs(L, kind):
+    """Launches per call: one per launch table (a table holds <= 40 params)."""
+    n = sum(1 for x in L.numel if x > 0)
+    return -(-n // 40)
+
+
+def run_e2e(args, z3, L, w, rep, stream, sid, step_bytes, world):
+    """The same step through the public API with host buffers: per step the
+    gradients go host->device from pinned memory and the updated bf16 shards
+    come back device->host, inside the timed region."""
+    import torch
+    k = max(3, min(args.steps, args.e2e_steps))
+    host_grads = torch.empty(rep.grads.shape, dtype=rep.grads.dtype, pin_memory=True)
+    host_grads.copy_(rep.grads)
+    host_out = torch.empty(rep.shards.shape, dtype=rep.shards.dtype, pin_memory=True)
+    h2d = host_grads.numel() * host_grads.element_size()
+    d2h = host_out.numel() * host_out.element_size()
+    for _ in range(2):
+        rep.grads.copy_(host_grads, non_blocking=True)
+        rep.step += 1
+        z3.z3_step_layer(L, rep.shards, rep.full, rep.grads, w.grad_stride, 1.0 / w.n_ranks,
+                         rep.master, rep.m, rep.v, HP, rep.step, stream=sid)
+        host_out.copy_(rep.shards, non_blocking=True)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(k):
+        rep.grads.copy_(host_grads, non_blocking=True)
+        rep.step += 1
+        z3.z3_step_layer(L, rep.shards, rep.full, rep.grads, w.grad_stride, 1.0 / w.n_ranks,
+                         rep.master, rep.m, rep.v, HP, rep.step, stream=sid)
+        host_out.copy_(rep.shards, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    return {"value": round(world * step_bytes * k / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k,
+            "ms_per_step": round(ms / k, 6)}
+
+
+# --------------------------------------------------------------------------
+# the oracle on the host cores
+# --------------------------------------------------------------------------
+
+def oracle_sample(w, n_elems: int, seed: int):
+    """A bounded sample of the workload for the CPU oracle: the first
+    n_elems elements of the layer's parameter list as one layer (same N_d,
+    same value distributions)."""
+    import numpy as np
+    import torch
+    from optimizer_state_gb300 import inputs as I
+    numel, left = [], n_elems
+    for n in w.numel:
+        take = min(n, left)
+        if take > 0:
+            numel.append(take)
+        left -= take
+    sw = I.Workload(w.name + "_sample", tuple((n,) for n in numel), w.n_ranks, w.param_std,
+                    w.grad_std)
+    gen = I.make_generator(seed, "cpu")
+    full = I.draw_master(sw, gen, "cpu").numpy()
+    grads = I.draw_grads(sw, gen, "cpu").view(torch.int16).numpy().view(np.uint16).reshape(-1)
+    return sw, full, grads
+
+
+def time_oracle(w, n_elems, min_seconds, max_steps, warmup=1, seed=0):
+    import oracle
+    sw, full, grads = oracle_sample(w, n_elems, seed)
+    O = oracle.layout(sw.numel, sw.n_ranks)
+    sh, ma, m, v = oracle.partition(O, full)
+    t = 0
+    for i in range(warmup):
+        t += 1
+        oracle.step_layer(O, sh, grads, sw.grad_stride, 1.0 / sw.n_ranks, ma, m, v, HP, t)
+    steps = 0
+    t0 = time.perf_counter()
+    while steps < max_steps and (steps == 0 or time.perf_counter() - t0 < min_seconds):
+        t += 1
+        oracle.step_layer(O, sh, grads, sw.grad_stride, 1.0 / sw.n_ranks, ma, m, v, HP, t)
+        steps += 1
+    dt = time.perf_counter() - t0
+    step_bytes = (2 * sw.n_ranks + 34) * O.psi
+    return dict(gbs=step_bytes * steps / dt / 1e9, params_per_s=O.psi * steps / dt, steps=steps,
+                seconds=dt, psi=O.psi, ms_per_step=1e3 * dt / steps)
+
+
+def cpu_baseline(seconds: float) -> dict:
+    from optimizer_state_gb300 import inputs as I
+    w = I.LAYER_D1024
+    r = time_oracle(w, w.psi, min_seconds=seconds, max_steps=10 ** 6)
+    return {"value": round(r["gbs"], 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "params_per_s": round(r["params_per_s"], 1),
+            "sample": f"{r['steps']} full layer steps of layer_d1024_nd8 (Psi={r['psi']}) "
+                      f"in {r['seconds']:.1f} s, single-threaded C oracle"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from optimizer_state_gb300 import inputs as I
+    w = I.LAYER_D1024
+    # size the per-step sample so that warmup + steps fit the time budget
+    probe = time_oracle(w, 1 << 20, min_seconds=0.0, max_steps=1, warmup=0)
+    per_elem_s = probe["seconds"] / probe["psi"]
+    budget = args.reference_seconds / max(1, args.steps + args.warmup)
+    n = int(min(w.psi, max(w.n_ranks * 8, budget / per_elem_s)))
+    r = time_oracle(w, n, min_seconds=0.0, max_steps=args.steps, warmup=args.warmup)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(r["gbs"], 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": r["steps"],
+        "warmup": args.warmup,
+        "ms_per_step": round(r["ms_per_step"], 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "layer_d1024_nd8", "psi": w.psi, "n_ranks": w.n_ranks,
+                   "sample_psi": r["psi"]},
+        "params_per_s": round(r["params_per_s"], 1),
+        "cpu_baseline": {"value": round(r["gbs"], 4), "unit": "GB/s", "cores": 1,
+                         "kind": "oracle",
+                         "sample": f"each step: the first {r['psi']} elements of the layer "
+                                   f"as one layer over N_d={w.n_ranks}"},
+        "e2e": {"value": round(r["gbs"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--kernel-steps", type=int, default=500)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cold-bytes", type=int, default=1536 << 20,
+                    help="total bytes of rotating state replicas")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-seconds", type=float, default=90.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if world != args.gpus:
+        if world == 1 and args.gpus > 1:
+            sys.exit("--gpus N > 1 must be launched with torchrun (one process per GPU)")
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_cuda(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,210 @@
+/*
+ * z3.h -- C ABI of the ZeRO-3 sharded model-state hot path on one GPU.
+ *
+ * The N logical data-parallel ranks of ZeRO stage 3 are held as shard
+ * regions of one GPU's memory, so the collectives are on-device data
+ * movement.  The operations follow the pages that define the method:
+ *
+ *   [ZD] "The ZeRO-3 Diagram Most People Remember Is Wrong" (duoan.github.io):
+ *        s.2 "The Actual Parameter Partition" (flatten, pad, contiguous slice
+ *        per rank) and s.3 "The Collectives You Should Expect" (AllGather
+ *        before forward and again before backward, ReduceScatter of the
+ *        gradients, the optimizer updates the local shard).
+ *   [S3] "ZeRO Stage 3: Parameter Partitioning" (mbrenndoerfer.com):
+ *        eq. M_Stage3 (16 bytes of model state per owned element) and the
+ *        communication list (2*Psi + 2*Psi + 2*Psi = 6*Psi bytes per step).
+ *   [ZS] "ZeRO Stages: Sharding Optimizer State, Gradients, and Parameters"
+ *        (mercemay.com): "Stage 2 also partitions gradients" (the reduce-
+ *        scatter sums across ranks and leaves each rank its slice; reduce per
+ *        micro-batch and accumulate the reduced slices).
+ *
+ * Notation: a layer is an ordered list of parameters; parameter p has n_p
+ * elements; N = n_ranks; s_p = ceil(n_p / N); rank r owns padded positions
+ * [r*s_p, (r+1)*s_p) of p (positions >= n_p are pad); o_p = sum_{q<p} s_q;
+ * F_p = sum_{q<p} n_q; S = sum_p s_p; Psi = sum_p n_p.
+ *
+ * Buffers (all device memory, all owned by the caller; the library never
+ * allocates or frees device memory):
+ *   shards   bf16 [N][S]   rank r's shard at r*S; p's slice at r*S + o_p
+ *   master, m, v, grad_shards   fp32 [N][S], same indexing
+ *   full     bf16 [Psi]    one gathered copy of the layer, parameters
+ *                          concatenated unpadded: p at F_p
+ *   grads    bf16 [N][grad_stride]   rank k's full gradient at k*grad_stride
+ * bf16 values travel as uint16_t bit patterns.  Pad positions of every
+ * [N][S] buffer are zero after z3_partition and stay zero under every other
+ * call.
+ *
+ * Conventions:
+ *   - Every call returns a z3_status; no call aborts, prints or traps, and
+ *     no device code asserts.  z3_last_error() gives the message of the
+ *     last failure on the calling thread.
+ *   - Device calls validate every argument on the host, then enqueue on the
+ *     caller's stream and return; a launch failure returns Z3_ERR_CUDA.
+ *     Errors during execution surface at the caller's next synchronisation.
+ *   - Device buffers must start on a 16-byte boundary (Z3_ERR_ALIGNMENT);
+ *     grad_stride must be a multiple of 8 elements (Z3_ERR_ALIGNMENT) and
+ *     >= Psi (Z3_ERR_INVALID_ARG).  Interior offsets (o_p, F_p, S) may be
+ *     anything.
+ *   - Output buffers must not overlap any other buffer of the same call
+ *     (Z3_ERR_INVALID_ARG), except the in-place state of the Adam calls.
+ *   - Calls make no synchronous CUDA calls and allocate nothing, so a caller
+ *     may capture them in a CUDA graph.
+ *   - A layout handle is immutable after creation and may be shared between
+ *     threads.
+ */
+#ifndef Z3_H
+#define Z3_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum z3_status {
+    Z3_OK = 0,
+    Z3_ERR_INVALID_ARG = 1, /* null/negative/inconsistent argument */
+    Z3_ERR_ALIGNMENT = 2,   /* buffer not 16-byte aligned, bad grad_stride */
+    Z3_ERR_OVERFLOW = 3,    /* a size does not fit int64 / the launch grid */
+    Z3_ERR_CUDA = 4         /* the CUDA runtime reported an error */
+} z3_status;
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *z3_stream;
+
+/* Opaque, library-owned host object describing one layer's layout. */
+typedef struct z3_layout z3_layout;
+
+/* Adam hyperparameters as real numbers.  Every constant of the update is
+ * rounded once to binary32 on the host: beta1, 1-beta1, beta2, 1-beta2,
+ * 1-beta1^t, 1-beta2^t, lr, eps and lr*weight_decay. */
+typedef struct z3_adam_hp {
+    double lr;
+    double beta1;
+    double beta2;
+    double eps;
+    double weight_decay; /* decoupled: p <- p - (lr*wd)*p before the step */
+} z3_adam_hp;
+
+/* Byte counts of one layer ([S3] communication list; per-kernel HBM bytes
+ * are the algorithmic bytes per unpadded element times Psi). */
+typedef struct z3_traffic {
+    int64_t psi;                 /* unpadded elements of the layer           */
+    int64_t ag_payload_bytes;    /* 2*Psi: one gathered bf16 copy            */
+    int64_t rs_payload_bytes;    /* 2*Psi: one bf16 gradient reduced         */
+    int64_t step_volume_bytes;   /* 6*Psi: AG fwd + AG bwd + RS ([S3])       */
+    int64_t dp_allreduce_bytes;  /* 2*Psi: plain data-parallel all-reduce    */
+    int64_t hbm_allgather;       /* 4*Psi       (read 2, write 2)            */
+    int64_t hbm_reduce_scatter;  /* (2N+4)*Psi  (read 2N, write 4)           */
+    int64_t hbm_reduce_scatter_accumulate; /* (2N+8)*Psi                     */
+    int64_t hbm_adam;            /* 30*Psi (read g,p,m,v 16; write p,m,v,b 14)*/
+    int64_t hbm_reduce_scatter_adam;       /* (2N+26)*Psi                    */
+    int64_t hbm_step_layer;      /* (2N+34)*Psi: AG + AG + fused RS/Adam     */
+    int64_t state_bytes_per_rank;/* 16*S ([S3] eq. M_Stage3, 2-byte grads)   */
+    int64_t state_bytes_per_rank_fp32_grad; /* 18*S ([ZS], 4-byte grads)     */
+} z3_traffic;
+
+/* ---- layout ([ZD] s.2; [ZS] "What stage 1 partitions") ---------------- */
+
+/* Builds the layout of a layer of n_params parameters with the given
+ * element counts over n_ranks logical ranks.  numel[p] >= 0 (0 is allowed:
+ * s_p = 0).  Errors: n_params < 1, n_ranks < 1, numel NULL or negative,
+ * out NULL (INVALID_ARG); N*S or Psi beyond int64 (OVERFLOW).  On success
+ * *out owns host memory released by z3_layout_destroy. */
+z3_status z3_layout_create(const int64_t *numel, int32_t n_params,
+                           int32_t n_ranks, z3_layout **out);
+
+/* Releases a layout (NULL is a no-op). */
+void z3_layout_destroy(z3_layout *layout);
+
+/* Scalar facts of a layout; any output pointer may be NULL. */
+z3_status z3_layout_info(const z3_layout *layout, int32_t *n_params,
+                         int32_t *n_ranks, int64_t *S, int64_t *psi,
+                         int64_t *psi_padded);
+
+/* Per-parameter arrays [n_params] (caller-owned host memory); any may be
+ * NULL. */
+z3_status z3_layout_params(const z3_layout *layout, int64_t *numel,
+                           int64_t *shard_numel, int64_t *shard_off,
+                           int64_t *full_off);
+
+/* Byte accounting of the layout ([S3] eq. M_Stage3 and communication list). */
+z3_status z3_stats(const z3_layout *layout, z3_traffic *out);
+
+/* ---- device operations ------------------------------------------------ */
+
+/* Initial partition ([ZD] s.2 steps 1-4; a broadcast-like step that runs
+ * once at initialisation, [ZD] s.3).  full: fp32 [Psi] (read).  Writes
+ * master[r][o_p+j] = full[F_p + r*s_p + j] (0 in the pad), m = v = 0 and
+ * shards = bf16 round-to-nearest-even of master.  All five buffers must be
+ * distinct and non-overlapping. */
+z3_status z3_partition(const z3_layout *layout, const float *full,
+                       uint16_t *shards, float *master, float *m, float *v,
+                       z3_stream stream);
+
+/* AllGather ([ZD] s.3; [S3] step 2): full[F_p + i] =
+ * shards[i / s_p][o_p + i mod s_p] for 0 <= i < n_p.  Bit copy; the pad is
+ * dropped.  shards is read; full [Psi] is written. */
+z3_status z3_allgather(const z3_layout *layout, const uint16_t *shards,
+                       uint16_t *full, z3_stream stream);
+
+/* ReduceScatter ([ZD] s.3; [ZS] "Stage 2 also partitions gradients"):
+ * for every owned position with padded index i = r*s_p + j < n_p,
+ *   g = fp32(grads[0][F_p+i]); g = g + fp32(grads[k][F_p+i]) for k = 1..N-1
+ *   (binary32, ascending rank order); g = g * scale;
+ *   grad_shards[r][o_p+j] = accumulate ? grad_shards[r][o_p+j] + g : g.
+ * Pad positions are written 0.  scale = 1/N gives the data-parallel mean.
+ * grads is read; grad_shards is written (and read when accumulate != 0). */
+z3_status z3_reduce_scatter(const z3_layout *layout, const uint16_t *grads,
+                            int64_t grad_stride, float *grad_shards,
+                            float scale, int32_t accumulate, z3_stream stream);
+
+/* Local-shard Adam ([ZD] s.3 "optimizer updates local shard"; Kingma & Ba,
+ * Algorithm 1) on every position of the [N][S] buffers, t = step >= 1:
+ *   m' = b1*m + c1*g;  v' = b2*v + c2*(g*g);  mh = m'/bc1;  vh = v'/bc2;
+ *   u = mh / (sqrt(vh) + eps);  p' = (p - lwd*p) - lr*u;  shards = bf16(p')
+ * in binary32 with IEEE-rounded division and square root, no fused
+ * multiply-add.  master, m, v are updated in place; grad_shards is read;
+ * shards is written.  Errors: hp NULL or non-finite, step < 1. */
+z3_status z3_adam_shard_step(const z3_layout *layout, float *master, float *m,
+                             float *v, const float *grad_shards,
+                             uint16_t *shards, const z3_adam_hp *hp,
+                             int64_t step, z3_stream stream);
+
+/* ReduceScatter fused with Adam: the reduced gradient of each owned
+ * position (as z3_reduce_scatter, accumulate into grad_acc when grad_acc is
+ * not NULL; pad positions get gradient 0) feeds the Adam update of that
+ * position in registers, so no fp32 gradient is written.  grad_acc (may be
+ * NULL) is read only.  Equivalent to z3_reduce_scatter into a copy of
+ * grad_acc followed by z3_adam_shard_step. */
+z3_status z3_reduce_scatter_adam(const z3_layout *layout,
+                                 const uint16_t *grads, int64_t grad_stride,
+                                 float scale, const float *grad_acc,
+                                 float *master, float *m, float *v,
+                                 uint16_t *shards, const z3_adam_hp *hp,
+                                 int64_t step, z3_stream stream);
+
+/* One layer step in the order of [ZD] s.3: forward AllGather into full,
+ * backward AllGather into full again, then the fused ReduceScatter + Adam
+ * that rewrites the shards.  Three kernel launches on the stream. */
+z3_status z3_step_layer(const z3_layout *layout, uint16_t *shards,
+                        uint16_t *full, const uint16_t *grads,
+                        int64_t grad_stride, float scale, float *master,
+                        float *m, float *v, const z3_adam_hp *hp,
+                        int64_t step, z3_stream stream);
+
+/* ---- errors ------------------------------------------------------------ */
+
+/* Static name of a status code. */
+const char *z3_status_string(z3_status status);
+
+/* Copies the message of the calling thread's last failure (NUL-terminated,
+ * truncated to len) into buf; returns the full message length. */
+size_t z3_last_error(char *buf, size_t len);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Z3_H */

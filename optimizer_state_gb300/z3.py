@@ -1,0 +1,250 @@
+"""Thin ctypes binding of the C ABI in ``include/z3.h``.
+
+Argument marshalling only: every step of the path runs in the CUDA library
+``_build/libz3.so``.  Functions keep the C names; device buffers may be
+passed as CUDA tensors (their data pointer is used; dtype and size are
+checked here, the library re-checks pointers, alignment and overlap) or as
+raw integer device addresses.  ``stream`` defaults to torch's current CUDA
+stream.  There is no CPU fallback: if the library is missing, loading fails
+with an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+Z3_OK, Z3_ERR_INVALID_ARG, Z3_ERR_ALIGNMENT, Z3_ERR_OVERFLOW, Z3_ERR_CUDA = range(5)
+
+# Every symbol include/z3.h declares.
+EXPORTS = ("z3_layout_create", "z3_layout_destroy", "z3_layout_info", "z3_layout_params",
+           "z3_stats", "z3_partition", "z3_allgather", "z3_reduce_scatter",
+           "z3_adam_shard_step", "z3_reduce_scatter_adam", "z3_step_layer",
+           "z3_status_string", "z3_last_error")
+
+
+class Z3Error(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_status_name(status)}: {message}")
+        self.status = status
+
+
+class AdamHP(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double),
+                ("beta2", ctypes.c_double), ("eps", ctypes.c_double),
+                ("weight_decay", ctypes.c_double)]
+
+
+class Traffic(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in (
+        "psi", "ag_payload_bytes", "rs_payload_bytes", "step_volume_bytes",
+        "dp_allreduce_bytes", "hbm_allgather", "hbm_reduce_scatter",
+        "hbm_reduce_scatter_accumulate", "hbm_adam", "hbm_reduce_scatter_adam",
+        "hbm_step_layer", "state_bytes_per_rank", "state_bytes_per_rank_fp32_grad")]
+
+    def as_dict(self) -> dict:
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Load the CUDA library (built by ``optimizer_state_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library {path} is not built; run "
+                               "`python -m optimizer_state_gb300.build` (no CPU fallback exists)")
+        lib = ctypes.CDLL(path)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        f32, st = ctypes.c_float, ctypes.c_int
+        hp = ctypes.POINTER(AdamHP)
+        sig = {
+            "z3_layout_create": (st, [vp, i32, i32, ctypes.POINTER(vp)]),
+            "z3_layout_destroy": (None, [vp]),
+            "z3_layout_info": (st, [vp, vp, vp, vp, vp, vp]),
+            "z3_layout_params": (st, [vp, vp, vp, vp, vp]),
+            "z3_stats": (st, [vp, ctypes.POINTER(Traffic)]),
+            "z3_partition": (st, [vp, vp, vp, vp, vp, vp, vp]),
+            "z3_allgather": (st, [vp, vp, vp, vp]),
+            "z3_reduce_scatter": (st, [vp, vp, i64, vp, f32, i32, vp]),
+            "z3_adam_shard_step": (st, [vp, vp, vp, vp, vp, vp, hp, i64, vp]),
+            "z3_reduce_scatter_adam": (st, [vp, vp, i64, f32, vp, vp, vp, vp, vp, hp, i64, vp]),
+            "z3_step_layer": (st, [vp, vp, vp, vp, i64, f32, vp, vp, vp, hp, i64, vp]),
+            "z3_status_string": (ctypes.c_char_p, [st]),
+            "z3_last_error": (ctypes.c_size_t, [ctypes.c_char_p, ctypes.c_size_t]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+        return lib
+
+
+def _status_name(status: int) -> str:
+    try:
+        return load().z3_status_string(status).decode()
+    except Exception:  # noqa: BLE001 - only used while formatting an error
+        return f"status {status}"
+
+
+def last_error() -> str:
+    lib = load()
+    buf = ctypes.create_string_buffer(1024)
+    lib.z3_last_error(buf, len(buf))
+    return buf.value.decode(errors="replace")
+
+
+def _check(status: int):
+    if status != Z3_OK:
+        raise Z3Error(status, last_error())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dev(t, dtypes, numel: int, name: str):
+    """Device address of a tensor (or a raw int address)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: needs >= {numel} elements, has {t.numel()}")
+    return t.data_ptr()
+
+
+def _dtypes():
+    import torch
+    return (torch.bfloat16, torch.int16, torch.uint16), (torch.float32,)
+
+
+class Layout:
+    """Owns a ``z3_layout`` handle (z3_layout_create / z3_layout_destroy)."""
+
+    def __init__(self, numel, n_ranks: int):
+        lib = load()
+        numel = [int(n) for n in numel]
+        arr = (ctypes.c_int64 * len(numel))(*numel)
+        h = ctypes.c_void_p()
+        _check(lib.z3_layout_create(ctypes.cast(arr, ctypes.c_void_p), len(numel), n_ranks,
+                                    ctypes.byref(h)))
+        self._h = h
+        self._lib = lib
+        P, N = ctypes.c_int32(), ctypes.c_int32()
+        S, psi, psip = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(lib.z3_layout_info(h, ctypes.byref(P), ctypes.byref(N), ctypes.byref(S),
+                                  ctypes.byref(psi), ctypes.byref(psip)))
+        self.n_params, self.n_ranks = P.value, N.value
+        self.S, self.psi, self.psi_padded = S.value, psi.value, psip.value
+        arrs = [(ctypes.c_int64 * self.n_params)() for _ in range(4)]
+        _check(lib.z3_layout_params(h, *[ctypes.cast(a, ctypes.c_void_p) for a in arrs]))
+        self.numel, self.shard_numel, self.shard_off, self.full_off = (list(a) for a in arrs)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def stats(self) -> dict:
+        t = Traffic()
+        _check(self._lib.z3_stats(self._h, ctypes.byref(t)))
+        return t.as_dict()
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.z3_layout_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 - interpreter shutdown
+            pass
+
+
+def _hp(hp) -> AdamHP:
+    if isinstance(hp, AdamHP):
+        return hp
+    return AdamHP(float(hp["lr"]), float(hp["beta1"]), float(hp["beta2"]), float(hp["eps"]),
+                  float(hp.get("weight_decay", 0.0)))
+
+
+def z3_partition(layout: Layout, full, shards, master, m, v, stream=None):
+    b16, f32 = _dtypes()
+    T = layout.psi_padded
+    _check(load().z3_partition(layout.handle, _dev(full, f32, layout.psi, "full"),
+                               _dev(shards, b16, T, "shards"), _dev(master, f32, T, "master"),
+                               _dev(m, f32, T, "m"), _dev(v, f32, T, "v"), _stream(stream)))
+
+
+def z3_allgather(layout: Layout, shards, full, stream=None):
+    b16, _ = _dtypes()
+    _check(load().z3_allgather(layout.handle, _dev(shards, b16, layout.psi_padded, "shards"),
+                               _dev(full, b16, layout.psi, "full"), _stream(stream)))
+
+
+def z3_reduce_scatter(layout: Layout, grads, grad_stride: int, grad_shards, scale: float,
+                      accumulate: bool = False, stream=None):
+    b16, f32 = _dtypes()
+    _check(load().z3_reduce_scatter(
+        layout.handle, _dev(grads, b16, layout.n_ranks * grad_stride, "grads"), grad_stride,
+        _dev(grad_shards, f32, layout.psi_padded, "grad_shards"), scale, 1 if accumulate else 0,
+        _stream(stream)))
+
+
+def z3_adam_shard_step(layout: Layout, master, m, v, grad_shards, shards, hp, step: int,
+                       stream=None):
+    b16, f32 = _dtypes()
+    T = layout.psi_padded
+    h = _hp(hp)
+    _check(load().z3_adam_shard_step(
+        layout.handle, _dev(master, f32, T, "master"), _dev(m, f32, T, "m"),
+        _dev(v, f32, T, "v"), _dev(grad_shards, f32, T, "grad_shards"),
+        _dev(shards, b16, T, "shards"), ctypes.byref(h), step, _stream(stream)))
+
+
+def z3_reduce_scatter_adam(layout: Layout, grads, grad_stride: int, scale: float, grad_acc,
+                           master, m, v, shards, hp, step: int, stream=None):
+    b16, f32 = _dtypes()
+    T = layout.psi_padded
+    h = _hp(hp)
+    _check(load().z3_reduce_scatter_adam(
+        layout.handle, _dev(grads, b16, layout.n_ranks * grad_stride, "grads"), grad_stride,
+        scale, _dev(grad_acc, f32, T, "grad_acc"), _dev(master, f32, T, "master"),
+        _dev(m, f32, T, "m"), _dev(v, f32, T, "v"), _dev(shards, b16, T, "shards"),
+        ctypes.byref(h), step, _stream(stream)))
+
+
+def z3_step_layer(layout: Layout, shards, full, grads, grad_stride: int, scale: float, master,
+                  m, v, hp, step: int, stream=None):
+    b16, f32 = _dtypes()
+    T = layout.psi_padded
+    h = _hp(hp)
+    _check(load().z3_step_layer(
+        layout.handle, _dev(shards, b16, T, "shards"), _dev(full, b16, layout.psi, "full"),
+        _dev(grads, b16, layout.n_ranks * grad_stride, "grads"), grad_stride, scale,
+        _dev(master, f32, T, "master"), _dev(m, f32, T, "m"), _dev(v, f32, T, "v"),
+        ctypes.byref(h), step, _stream(stream)))

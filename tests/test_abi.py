@@ -1,0 +1,142 @@
+"""C-ABI library on the CPU: it builds for sm_103a, loads, exports every
+symbol include/z3.h declares, and its host logic (layout, accounting,
+argument validation) agrees with the oracle.  No kernel is launched here:
+every device call below fails validation before reaching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from optimizer_state_gb300 import build as z3build
+from optimizer_state_gb300 import z3
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    z3build.build()
+    return z3.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "z3.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(z3_[a-z_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert len(names) >= 13
+    assert sorted(z3.EXPORTS) == names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert lib.z3_status_string(0) == b"Z3_OK"
+    assert lib.z3_status_string(2) == b"Z3_ERR_ALIGNMENT"
+
+
+CASES = [([35, 13, 12], 4), ([12584960 // 4] * 4, 8), ([0, 5, 0, 7], 3), ([1], 64),
+         ([262147], 2), ([262147], 64), ([3, 0], 1), ([50257 * 1024], 16)]
+
+
+@pytest.mark.parametrize("numel,n_ranks", CASES)
+def test_layout_matches_oracle(lib, orc, numel, n_ranks):
+    L = z3.Layout(numel, n_ranks)
+    O = orc.layout(numel, n_ranks)
+    assert (L.S, L.psi, L.psi_padded) == (O.S, O.psi, O.psi_padded)
+    assert L.shard_numel == list(O.shard_numel)
+    assert L.shard_off == list(O.shard_off)
+    assert L.full_off == list(O.full_off)
+    assert L.numel == list(O.numel)
+    st = L.stats()
+    acc = orc.accounting(O)
+    assert st["state_bytes_per_rank"] == acc["state_bytes_per_rank"]
+    assert st["state_bytes_per_rank_fp32_grad"] == acc["state_bytes_per_rank_fp32_grad"]
+    assert st["step_volume_bytes"] == acc["step_volume_bytes"]
+    assert st["dp_allreduce_bytes"] == acc["dp_volume_bytes"]
+    N = n_ranks
+    assert st["hbm_step_layer"] == (2 * N + 34) * L.psi
+    assert st["hbm_reduce_scatter_adam"] == (2 * N + 26) * L.psi
+
+
+def test_layout_errors(lib):
+    with pytest.raises(z3.Z3Error) as e:
+        z3.Layout([5], 0)
+    assert e.value.status == z3.Z3_ERR_INVALID_ARG and "n_ranks" in str(e.value)
+    with pytest.raises(z3.Z3Error) as e:
+        z3.Layout([5, -1], 4)
+    assert e.value.status == z3.Z3_ERR_INVALID_ARG
+    with pytest.raises(z3.Z3Error) as e:
+        z3.Layout([2 ** 62, 2 ** 62], 1)
+    assert e.value.status == z3.Z3_ERR_OVERFLOW
+    out = ctypes.c_void_p()
+    assert lib.z3_layout_create(None, 1, 1, ctypes.byref(out)) == z3.Z3_ERR_INVALID_ARG
+    arr = (ctypes.c_int64 * 1)(5)
+    assert lib.z3_layout_create(ctypes.cast(arr, ctypes.c_void_p), 0, 1,
+                                ctypes.byref(out)) == z3.Z3_ERR_INVALID_ARG
+    assert lib.z3_layout_info(None, None, None, None, None, None) == z3.Z3_ERR_INVALID_ARG
+    lib.z3_layout_destroy(None)  # no-op
+
+
+def test_device_call_validation_without_gpu(lib):
+    """Host-side checks return before any CUDA call (fake device addresses)."""
+    L = z3.Layout([35, 13, 12], 4)
+    A = 1 << 32                       # an aligned fake address
+    far = A + (1 << 28)
+    st = lambda s: (s, z3.last_error())  # noqa: E731
+    # NULL / misaligned / overlapping buffers
+    s, msg = st(lib.z3_allgather(L.handle, None, A, None))
+    assert s == z3.Z3_ERR_INVALID_ARG and "shards" in msg
+    s, msg = st(lib.z3_allgather(L.handle, A + 2, far, None))
+    assert s == z3.Z3_ERR_ALIGNMENT
+    s, msg = st(lib.z3_allgather(L.handle, A, A + 16, None))
+    assert s == z3.Z3_ERR_INVALID_ARG and "overlaps" in msg
+    # grad_stride rules
+    s, msg = st(lib.z3_reduce_scatter(L.handle, A, 59, far, 0.25, 0, None))
+    assert s == z3.Z3_ERR_INVALID_ARG and "grad_stride" in msg
+    s, msg = st(lib.z3_reduce_scatter(L.handle, A, 61, far, 0.25, 0, None))
+    assert s == z3.Z3_ERR_ALIGNMENT
+    s, msg = st(lib.z3_reduce_scatter(L.handle, A, 64, far, float("nan"), 0, None))
+    assert s == z3.Z3_ERR_INVALID_ARG
+    # Adam: step and hyperparameters
+    hp = z3.AdamHP(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    bufs = [A + i * (1 << 24) for i in range(5)]
+    s, msg = st(lib.z3_adam_shard_step(L.handle, *bufs, ctypes.byref(hp), 0, None))
+    assert s == z3.Z3_ERR_INVALID_ARG and "step" in msg
+    bad = z3.AdamHP(float("inf"), 0.9, 0.999, 1e-8, 0.0)
+    s, msg = st(lib.z3_adam_shard_step(L.handle, *bufs, ctypes.byref(bad), 1, None))
+    assert s == z3.Z3_ERR_INVALID_ARG
+    s, msg = st(lib.z3_adam_shard_step(L.handle, *bufs, None, 1, None))
+    assert s == z3.Z3_ERR_INVALID_ARG
+    s, msg = st(lib.z3_step_layer(None, *bufs[:2], A, 64, 0.25, *bufs[2:], ctypes.byref(hp),
+                                  1, None))
+    assert s == z3.Z3_ERR_INVALID_ARG
+    s, msg = st(lib.z3_reduce_scatter_adam(L.handle, A, 64, 0.25, None, A, far, far + 4096,
+                                           far + 8192, ctypes.byref(hp), 1, None))
+    assert s == z3.Z3_ERR_INVALID_ARG and "overlaps" in msg
+
+
+def test_zero_size_layer_is_a_noop(lib):
+    L = z3.Layout([0, 0], 4)
+    assert (L.S, L.psi, L.psi_padded) == (0, 0, 0)
+    assert lib.z3_allgather(L.handle, None, None, None) == z3.Z3_OK
+    assert lib.z3_partition(L.handle, None, None, None, None, None, None) == z3.Z3_OK
+
+
+def test_product_never_reaches_the_oracle():
+    """The package and its CUDA sources import, include or link nothing from
+    oracle/; the oracle imports nothing from the package."""
+    pkg = os.path.join(ROOT, "optimizer_state_gb300")
+    pat = re.compile(r"^\s*(import\s+oracle|from\s+oracle|#\s*include\s*[<\"].*oracle)", re.M)
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cpp", ".h")):
+                assert not pat.search(open(os.path.join(dirpath, f)).read()), f
+    back = re.compile(r"^\s*(import|from)\s+optimizer_state_gb300", re.M)
+    for f in os.listdir(os.path.join(ROOT, "oracle")):
+        if f.endswith((".py", ".c")):
+            assert not back.search(open(os.path.join(ROOT, "oracle", f)).read()), f
