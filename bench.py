@@ -387,7 +387,10 @@ def time_oracle(w, n_elems, min_seconds, max_steps, warmup=1, seed=0):
         oracle.step_layer(O, sh, grads, sw.grad_stride, 1.0 / sw.n_ranks, ma, m, v, HP, t)
     steps = 0
     t0 = time.perf_counter()
-    while steps < max_steps and (steps == 0 or time.perf_counter() - t0 < min_seconds):
+    # exactly max_steps steps, or (with min_seconds > 0) until min_seconds pass
+    while steps < max_steps:
+        if min_seconds > 0 and steps > 0 and time.perf_counter() - t0 >= min_seconds:
+            break
         t += 1
         oracle.step_layer(O, sh, grads, sw.grad_stride, 1.0 / sw.n_ranks, ma, m, v, HP, t)
         steps += 1

@@ -78,7 +78,7 @@ typedef struct z3_layout z3_layout;
 
 /* Adam hyperparameters as real numbers.  Every constant of the update is
  * rounded once to binary32 on the host: beta1, 1-beta1, beta2, 1-beta2,
- * 1-beta1^t, 1-beta2^t, lr, eps and lr*weight_decay. */
+ * 1/(1-beta1^t), 1/(1-beta2^t), lr, eps and lr*weight_decay. */
 typedef struct z3_adam_hp {
     double lr;
     double beta1;
@@ -162,9 +162,10 @@ z3_status z3_reduce_scatter(const z3_layout *layout, const uint16_t *grads,
 
 /* Local-shard Adam ([ZD] s.3 "optimizer updates local shard"; Kingma & Ba,
  * Algorithm 1) on every position of the [N][S] buffers, t = step >= 1:
- *   m' = b1*m + c1*g;  v' = b2*v + c2*(g*g);  mh = m'/bc1;  vh = v'/bc2;
+ *   m' = b1*m + c1*g;  v' = b2*v + c2*(g*g);  mh = m'*rb1;  vh = v'*rb2;
  *   u = mh / (sqrt(vh) + eps);  p' = (p - lwd*p) - lr*u;  shards = bf16(p')
- * in binary32 with IEEE-rounded division and square root, no fused
+ * (rb1 = 1/(1-beta1^t), rb2 = 1/(1-beta2^t): the bias corrections) in
+ * binary32 with IEEE-rounded division and square root, no fused
  * multiply-add.  master, m, v are updated in place; grad_shards is read;
  * shards is written.  Errors: hp NULL or non-finite, step < 1. */
 z3_status z3_adam_shard_step(const z3_layout *layout, float *master, float *m,

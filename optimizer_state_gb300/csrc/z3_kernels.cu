@@ -97,15 +97,15 @@ __device__ __forceinline__ uint4 window8(const uint4 &lo, const uint4 &hi) {
 
 // Binary32 constants of one Adam step (each rounded once on the host).
 struct AdamK {
-    float b1, c1, b2, c2, bc1, bc2, lr, eps, lwd;
+    float b1, c1, b2, c2, rb1, rb2, lr, eps, lwd;
 };
 
 // Kingma & Ba, Algorithm 1, in the order fixed by include/z3.h.
 __device__ __forceinline__ void adam1(float g, float &p, float &m, float &v, const AdamK &k) {
     const float m1 = __fadd_rn(__fmul_rn(k.b1, m), __fmul_rn(k.c1, g));
     const float v1 = __fadd_rn(__fmul_rn(k.b2, v), __fmul_rn(k.c2, __fmul_rn(g, g)));
-    const float mh = __fdiv_rn(m1, k.bc1);
-    const float vh = __fdiv_rn(v1, k.bc2);
+    const float mh = __fmul_rn(m1, k.rb1);
+    const float vh = __fmul_rn(v1, k.rb2);
     const float u = __fdiv_rn(mh, __fadd_rn(__fsqrt_rn(vh), k.eps));
     const float pd = __fsub_rn(p, __fmul_rn(k.lwd, p));
     p = __fsub_rn(pd, __fmul_rn(k.lr, u));
@@ -272,16 +272,9 @@ __device__ __forceinline__ void finish1(const ReduceArgs &a, int64_t x, float g,
 template <int PHI, int MODE>
 __device__ __forceinline__ void reduce_vector(const ReduceArgs &a, int n_ranks, int64_t x0,
                                               int64_t delta) {
-    // State the epilogue needs, loaded first so it is in flight with the
-    // gradient loads.
-    float st0[8], st1[8], st2[8], st3[8];
-    if constexpr (MODE == kRSAcc) ld8f(a.out + x0, st0);
-    if constexpr (MODE >= kRSAdam) {
-        ld8f(a.master + x0, st0);
-        ld8f(a.m + x0, st1);
-        ld8f(a.v + x0, st2);
-        if constexpr (MODE == kRSAccAdam) ld8f(a.acc_in + x0, st3);
-    }
+    // Rank fold first (8 ranks' 16-byte loads in flight per batch), then the
+    // epilogue state: keeping the state out of the fold keeps the kernel
+    // within 64 registers, and the other resident warps cover its latency.
     const uint16_t *gp = a.grads + (x0 + delta - PHI);
     float acc[8];
     for (int k0 = 0; k0 < n_ranks; k0 += kRankBatch) {
@@ -315,24 +308,32 @@ __device__ __forceinline__ void reduce_vector(const ReduceArgs &a, int n_ranks, 
     if constexpr (MODE == kRS) {
         st8f(a.out + x0, g);
     } else if constexpr (MODE == kRSAcc) {
+        float o[8];
+        ld8f(a.out + x0, o);
 #pragma unroll
-        for (int l = 0; l < 8; ++l) g[l] = __fadd_rn(st0[l], g[l]);
+        for (int l = 0; l < 8; ++l) g[l] = __fadd_rn(o[l], g[l]);
         st8f(a.out + x0, g);
     } else {
+        float p[8], m[8], v[8];
+        ld8f(a.master + x0, p);
+        ld8f(a.m + x0, m);
+        ld8f(a.v + x0, v);
         if constexpr (MODE == kRSAccAdam) {
+            float c[8];
+            ld8f(a.acc_in + x0, c);
 #pragma unroll
-            for (int l = 0; l < 8; ++l) g[l] = __fadd_rn(st3[l], g[l]);
+            for (int l = 0; l < 8; ++l) g[l] = __fadd_rn(c[l], g[l]);
         }
 #pragma unroll
-        for (int l = 0; l < 8; ++l) adam1(g[l], st0[l], st1[l], st2[l], a.k);
-        st8f(a.master + x0, st0);
-        st8f(a.m + x0, st1);
-        st8f(a.v + x0, st2);
+        for (int l = 0; l < 8; ++l) adam1(g[l], p[l], m[l], v[l], a.k);
+        st8f(a.master + x0, p);
+        st8f(a.m + x0, m);
+        st8f(a.v + x0, v);
         uint4 b;
-        b.x = pack_bf16x2(st0[0], st0[1]);
-        b.y = pack_bf16x2(st0[2], st0[3]);
-        b.z = pack_bf16x2(st0[4], st0[5]);
-        b.w = pack_bf16x2(st0[6], st0[7]);
+        b.x = pack_bf16x2(p[0], p[1]);
+        b.y = pack_bf16x2(p[2], p[3]);
+        b.z = pack_bf16x2(p[4], p[5]);
+        b.w = pack_bf16x2(p[6], p[7]);
         *reinterpret_cast<uint4 *>(a.shards + x0) = b;
     }
 }
@@ -397,6 +398,56 @@ k_reduce(const __grid_constant__ Tab tab, const ReduceArgs a) {
             default: reduce_tile<7, MODE>(a, n_ranks, c0, c_end, valid_end, delta, qbeg, qend); break;
         }
     }
+}
+
+// --------------------------------------------------------------------------
+// Reduce for tables whose chunks all have phase 0 (every transformer layout
+// whose parameter sizes divide by 8N).  One vector per thread; the kernel is
+// kept at <= 64 registers so that four 256-thread CTAs (32 warps) share an
+// SM: with eight 16-byte gradient loads and six 16-byte state loads in
+// flight per thread, that is enough memory-level parallelism to hide HBM
+// latency while the Adam arithmetic of other warps runs.
+// --------------------------------------------------------------------------
+
+// Element-wise handling of a vector at a chunk edge or in the pad (rare: at
+// most two vectors per chunk), kept out of line so that it does not raise
+// the register count of the vector path.
+template <int MODE>
+__device__ __noinline__ void reduce_edges(const ReduceArgs a, int n_ranks, int64_t x0,
+                                          int64_t delta, int64_t c0, int64_t c_end,
+                                          int64_t valid_end) {
+    for (int l = 0; l < kVec; ++l) {
+        const int64_t x = x0 + l;
+        if (x < c0 || x >= c_end) continue;  // another chunk's element
+        const bool pad = x >= valid_end;
+        float g = 0.0f;
+        if (!pad) {
+            const uint16_t *gp = a.grads + (x + delta);
+            float s = bf16_to_f32(gp[0]);
+            for (int k = 1; k < n_ranks; ++k)
+                s = __fadd_rn(s, bf16_to_f32(gp[(int64_t)k * a.stride]));
+            g = __fmul_rn(s, a.scale);
+        }
+        finish1<MODE>(a, x, g, pad);
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kReduceThreads, 4)
+k_reduce_aligned(const __grid_constant__ Tab tab, const ReduceArgs a) {
+    static_assert(kReduceVecPerThread == 1, "one vector per thread");
+    const TileRef tr = locate(tab, blockIdx.x);
+    const TabEntry &e = tab.e[tr.p];
+    const int64_t c0 = tr.r * tab.S + e.o;
+    const int64_t c_end = c0 + e.s;
+    const int64_t valid_end = c0 + min(e.s, max((int64_t)0, e.n - tr.r * e.s));
+    const int64_t delta = e.F + tr.r * e.s - c0;
+    const int64_t x0 = (c0 / kVec + tr.t * (int64_t)kReduceThreads + threadIdx.x) * kVec;
+    if (x0 >= c_end) return;  // past the chunk's last vector
+    if (x0 >= c0 && x0 + kVec <= valid_end)
+        reduce_vector<0, MODE>(a, tab.n_ranks, x0, delta);
+    else
+        reduce_edges<MODE>(a, tab.n_ranks, x0, delta, c0, c_end, valid_end);
 }
 
 // --------------------------------------------------------------------------
@@ -534,8 +585,8 @@ z3_status adam_constants(const char *fn, const z3_adam_hp *hp, int64_t step, Ada
     k->c1 = (float)(1.0 - hp->beta1);
     k->b2 = (float)hp->beta2;
     k->c2 = (float)(1.0 - hp->beta2);
-    k->bc1 = (float)(1.0 - std::pow(hp->beta1, (double)step));
-    k->bc2 = (float)(1.0 - std::pow(hp->beta2, (double)step));
+    k->rb1 = (float)(1.0 / (1.0 - std::pow(hp->beta1, (double)step)));
+    k->rb2 = (float)(1.0 / (1.0 - std::pow(hp->beta2, (double)step)));
     k->lr = (float)hp->lr;
     k->eps = (float)hp->eps;
     k->lwd = (float)(hp->lr * hp->weight_decay);
@@ -563,22 +614,25 @@ z3_status run_allgather(const z3_layout *L, const uint16_t *shards, uint16_t *fu
 }
 
 template <int MODE>
-void launch_reduce(const Tab &t, const ReduceArgs &a, cudaStream_t stream) {
+z3_status launch_reduce(const Tab &t, const ReduceArgs &a, cudaStream_t stream) {
     if (t.phase0)
-        k_reduce<true, MODE><<<(unsigned)t.tiles, kReduceThreads, 0, stream>>>(t, a);
+        k_reduce_aligned<MODE><<<(unsigned)t.tiles, kReduceThreads, 0, stream>>>(t, a);
     else
         k_reduce<false, MODE><<<(unsigned)t.tiles, kReduceThreads, 0, stream>>>(t, a);
+    return Z3_OK;
 }
 
 z3_status run_reduce(const z3_layout *L, const ReduceArgs &a, int mode, cudaStream_t stream,
                      const char *fn) {
     for (const Tab &t : L->reduce_tabs) {
+        z3_status st;
         switch (mode) {
-            case kRS: launch_reduce<kRS>(t, a, stream); break;
-            case kRSAcc: launch_reduce<kRSAcc>(t, a, stream); break;
-            case kRSAdam: launch_reduce<kRSAdam>(t, a, stream); break;
-            default: launch_reduce<kRSAccAdam>(t, a, stream); break;
+            case kRS: st = launch_reduce<kRS>(t, a, stream); break;
+            case kRSAcc: st = launch_reduce<kRSAcc>(t, a, stream); break;
+            case kRSAdam: st = launch_reduce<kRSAdam>(t, a, stream); break;
+            default: st = launch_reduce<kRSAccAdam>(t, a, stream); break;
         }
+        if (st != Z3_OK) return st;
     }
     return launched(fn);
 }

@@ -191,7 +191,7 @@ def allreduce(L: Layout, grads: np.ndarray, grad_stride: int, scale: float) -> n
     return out
 
 
-ADAM_CONSTANT_NAMES = ("b1", "c1", "b2", "c2", "bc1", "bc2", "lr", "eps", "lwd")
+ADAM_CONSTANT_NAMES = ("b1", "c1", "b2", "c2", "rb1", "rb2", "lr", "eps", "lwd")
 
 
 def adam_constants(lr, beta1, beta2, eps, weight_decay, step) -> dict:

@@ -258,15 +258,17 @@ void or_allreduce(int64_t psi, int32_t n_ranks, const uint16_t *grads,
 /* The hyperparameters are real numbers (double); every constant the update */
 /* uses is rounded once to binary32:                                        */
 /*   b1 = f(beta1), c1 = f(1 - beta1), b2 = f(beta2), c2 = f(1 - beta2),    */
-/*   bc1 = f(1 - beta1^t), bc2 = f(1 - beta2^t), lr = f(lr), eps = f(eps),  */
-/*   lwd = f(lr * weight_decay).                                            */
-/* Update (Kingma & Ba, Algorithm 1, in binary32, in this order):           */
+/*   rb1 = f(1 / (1 - beta1^t)), rb2 = f(1 / (1 - beta2^t)),                */
+/*   lr = f(lr), eps = f(eps), lwd = f(lr * weight_decay).                  */
+/* Update (Kingma & Ba, Algorithm 1, in binary32, in this order; the bias   */
+/* corrections m/(1-beta1^t) and v/(1-beta2^t) are applied as products with */
+/* their reciprocals, which is the same quantity in exact arithmetic):      */
 /*   m' = b1*m + c1*g;  v' = b2*v + c2*(g*g)                                */
-/*   mh = m'/bc1;  vh = v'/bc2;  u = mh / (sqrt(vh) + eps)                  */
+/*   mh = m'*rb1;  vh = v'*rb2;  u = mh / (sqrt(vh) + eps)                  */
 /*   p' = (p - lwd*p) - lr*u;  bf16 = RNE(p')                               */
 /* ------------------------------------------------------------------------ */
 typedef struct {
-    float b1, c1, b2, c2, bc1, bc2, lr, eps, lwd;
+    float b1, c1, b2, c2, rb1, rb2, lr, eps, lwd;
 } adam_consts;
 
 static adam_consts adam_constants(double lr, double beta1, double beta2,
@@ -278,8 +280,8 @@ static adam_consts adam_constants(double lr, double beta1, double beta2,
     k.c1 = (float)(1.0 - beta1);
     k.b2 = (float)beta2;
     k.c2 = (float)(1.0 - beta2);
-    k.bc1 = (float)(1.0 - pow(beta1, (double)step));
-    k.bc2 = (float)(1.0 - pow(beta2, (double)step));
+    k.rb1 = (float)(1.0 / (1.0 - pow(beta1, (double)step)));
+    k.rb2 = (float)(1.0 / (1.0 - pow(beta2, (double)step)));
     k.lr = (float)lr;
     k.eps = (float)eps;
     k.lwd = (float)(lr * weight_decay);
@@ -295,8 +297,8 @@ void or_adam_constants(double lr, double beta1, double beta2, double eps,
     out9[1] = k.c1;
     out9[2] = k.b2;
     out9[3] = k.c2;
-    out9[4] = k.bc1;
-    out9[5] = k.bc2;
+    out9[4] = k.rb1;
+    out9[5] = k.rb2;
     out9[6] = k.lr;
     out9[7] = k.eps;
     out9[8] = k.lwd;
@@ -312,8 +314,8 @@ void or_adam(int64_t n, float *master, float *m, float *v, const float *grad,
         float p = master[i];
         float m1 = k.b1 * m[i] + k.c1 * g;
         float v1 = k.b2 * v[i] + k.c2 * (g * g);
-        float mh = m1 / k.bc1;
-        float vh = v1 / k.bc2;
+        float mh = m1 * k.rb1;
+        float vh = v1 * k.rb2;
         float u = mh / (sqrtf(vh) + k.eps);
         float pd = p - k.lwd * p;
         float p1 = pd - k.lr * u;

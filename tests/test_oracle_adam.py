@@ -84,8 +84,8 @@ def test_constants_are_rounded_once(orc):
     particular 1 - beta2 is not formed from an already-rounded beta2."""
     for step in (1, 2, 10, 1000):
         k = orc.adam_constants(1e-3, 0.9, 0.999, 1e-8, 0.1, step)
-        assert k["bc1"] == np.float32(1 - 0.9 ** step)
-        assert k["bc2"] == np.float32(1 - 0.999 ** step)
+        assert k["rb1"] == np.float32(1 / (1 - 0.9 ** step))
+        assert k["rb2"] == np.float32(1 / (1 - 0.999 ** step))
         assert k["c2"] == np.float32(0.001) and k["c2"] != np.float32(1) - np.float32(0.999)
         assert k["lwd"] == np.float32(1e-4)
     with pytest.raises(ValueError):
