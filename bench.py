@@ -49,6 +49,22 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest rank's time (the timed region ends when every rank ends)."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(world: int, step_bytes: int, steps: int, ms_max: float) -> float:
+    """Whole-job GB/s: every rank ran `steps` steps of `step_bytes` each."""
+    return world * step_bytes * steps / (ms_max * 1e-3) / 1e9
+
+
 def measured_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -246,13 +262,9 @@ def run_cuda(args, world, rank, local):
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, z3, L, w, reps[0], stream, sid, step_bytes, world)
 
-    ms_max = ms_total
-    if world > 1:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks(ms_total, world, dev)
     ms_step = ms_max / args.steps
-    value = world * step_bytes * args.steps / (ms_max * 1e-3) / 1e9
+    value = aggregate_gbs(world, step_bytes, args.steps, ms_max)
 
     if rank == 0:
         peak, peak_kind = measured_hbm_peak()
@@ -288,7 +300,7 @@ def run_cuda(args, world, rank, local):
             "pct_of_8tbs": round(100.0 * value / (NOMINAL_HBM_GBS * world), 2),
             "kernels_ms": {"allgather": round(t_ag, 6), "reduce_scatter_adam": round(t_rs, 6)},
             "roofline": {
-                "kernel": "k_reduce<aligned, RS+Adam> (fused reduce-scatter + Adam)",
+                "kernel": "k_reduce_aligned<RSAdam> (fused reduce-scatter + Adam)",
                 "bound": "hbm",
                 "achieved": round(achieved, 2),
                 "peak": peak,
