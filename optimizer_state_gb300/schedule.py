@@ -1,0 +1,95 @@
+"""Multi-layer ZeRO-3 step: the schedule of "The ZeRO-3 Diagram Most People
+Remember Is Wrong", s.3 over a whole model.
+
+Forward: AllGather of every unit (layer or embedding) in order.  Backward:
+for every unit in reverse order, AllGather again, then the fused
+reduce-scatter + Adam of that unit ("ZeRO Stage 3: Parameter Partitioning":
+the backward pass traverses layers in reverse).  Every gather lands in ONE
+transient buffer sized for the largest unit (same page: the transient buffer
+is bounded by the largest single layer).
+
+Argument marshalling and launch ordering only; every step runs in the CUDA
+library through :mod:`optimizer_state_gb300.z3`.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import inputs as I
+from . import z3
+
+
+class Unit:
+    """Sharded state of one unit (a layer or the embedding)."""
+
+    def __init__(self, w: I.Workload, dev, gen: torch.Generator | None, grads: bool = True):
+        self.w = w
+        self.L = z3.Layout(w.numel, w.n_ranks)
+        T = self.L.psi_padded
+        self.shards = torch.empty(T, dtype=torch.bfloat16, device=dev)
+        self.master = torch.empty(T, dtype=torch.float32, device=dev)
+        self.m = torch.empty(T, dtype=torch.float32, device=dev)
+        self.v = torch.empty(T, dtype=torch.float32, device=dev)
+        self.grads = None
+        if gen is not None:
+            full = I.draw_master(w, gen, dev).to(dev)
+            z3.z3_partition(self.L, full, self.shards, self.master, self.m, self.v)
+            del full
+            if grads:
+                self.grads = I.draw_grads(w, gen, dev).to(dev)
+
+    @property
+    def step_bytes(self) -> int:
+        return self.L.stats()["hbm_step_layer"]
+
+
+class Model:
+    """All units of a model plus the shared transient gathered buffer."""
+
+    def __init__(self, units: list[Unit], dev):
+        self.units = units
+        self.dev = dev
+        self.full = torch.empty(max(u.L.psi for u in units), dtype=torch.bfloat16, device=dev)
+        self.t = 0
+
+    @property
+    def psi(self) -> int:
+        return sum(u.L.psi for u in self.units)
+
+    @property
+    def step_bytes(self) -> int:
+        return sum(u.step_bytes for u in self.units)
+
+    def launches_per_step(self) -> int:
+        n = 0
+        for u in self.units:
+            tabs = -(-sum(1 for x in u.L.numel if x > 0) // 40)
+            n += 3 * tabs
+        return n
+
+    def step(self, hp: dict, stream=None, t: int | None = None, on_gather=None):
+        """One training step.  `on_gather(phase, index)` (optional) is called
+        after each gather is enqueued, with the transient buffer holding that
+        unit's parameters once the stream reaches it -- the point where the
+        forward or backward compute of the unit would run."""
+        if t is None:
+            self.t += 1
+            t = self.t
+        for i, u in enumerate(self.units):            # forward
+            z3.z3_allgather(u.L, u.shards, self.full, stream=stream)
+            if on_gather is not None:
+                on_gather("forward", i)
+        for i in range(len(self.units) - 1, -1, -1):    # backward, reverse order
+            u = self.units[i]
+            z3.z3_allgather(u.L, u.shards, self.full, stream=stream)
+            if on_gather is not None:
+                on_gather("backward", i)
+            z3.z3_reduce_scatter_adam(u.L, u.grads, u.w.grad_stride, 1.0 / u.w.n_ranks, None,
+                                      u.master, u.m, u.v, u.shards, hp, t, stream=stream)
+
+
+def full_step_model(dev, seed: int = 0) -> Model:
+    """The 24-layer d=1024 model with its [50257, 1024] embedding, N_d = 16."""
+    gen = I.make_generator(seed, dev)
+    return Model([Unit(w, dev, gen) for w in I.full_step_units()], dev)
+

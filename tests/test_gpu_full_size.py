@@ -1,0 +1,229 @@
+"""Parity at the full sizes of the larger workloads, in the launch
+configuration bench.py uses: the 7B-style layer at N_d = 8 and 64, the
+24-layer full step at N_d = 16, and the prime-length sweep with four
+micro-batches (including the largest points).  The oracle computes a sample
+of outputs one by one from the input bytes read back at those positions:
+every rank's first and last owned element of every parameter, both sides of
+every pad boundary, and random positions.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import (bits32, f32, gather_rows, pick, sampled_shard_positions,
+                         shard_to_full, u16)
+from optimizer_state_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+
+
+@pytest.fixture(scope="module")
+def z3mod():
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA is not available: the GPU tests need a GPU")
+    from optimizer_state_gb300 import build, z3
+    build.build()
+    z3.load()
+    return z3
+
+
+@pytest.fixture(autouse=True)
+def _free_memory():
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+class Probe:
+    """State of one layer at sampled shard positions, before a step."""
+
+    def __init__(self, orc, O, shards, master, m, v, n_random=1 << 20, seed=0):
+        self.O = O
+        self.xs = sampled_shard_positions(O, n_random, seed)
+        self.e, self.valid = shard_to_full(O, self.xs)
+        self.shards = u16(pick(shards, self.xs))
+        self.master = f32(pick(master, self.xs))
+        self.m = f32(pick(m, self.xs))
+        self.v = f32(pick(v, self.xs))
+
+    def expected(self, orc, grads, stride, scale, hp, t, acc=None):
+        """Oracle outputs at the sampled positions after one fused
+        reduce-scatter + Adam (acc: running sums at the positions, or None)."""
+        O, ev = self.O, self.e[self.valid]
+        nv = int(ev.size)
+        G = np.ascontiguousarray(gather_rows(grads, O.n_ranks, stride, ev))
+        fold = orc.allreduce(orc.layout([nv], O.n_ranks), G.reshape(-1), nv, scale)
+        g = np.zeros(self.xs.size, np.float32)
+        g[self.valid] = fold
+        if acc is not None:
+            g[self.valid] = (acc[self.valid] + g[self.valid]).astype(np.float32)
+        p, m, v = self.master.copy(), self.m.copy(), self.v.copy()
+        bf = np.zeros(self.xs.size, np.uint16)
+        orc.adam(p, m, v, g, bf, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"],
+                 hp["weight_decay"], t)
+        return dict(master=p, m=m, v=v, shards=bf)
+
+    def check_after(self, want, shards, master, m, v):
+        got = dict(shards=u16(pick(shards, self.xs)), master=f32(pick(master, self.xs)),
+                   m=f32(pick(m, self.xs)), v=f32(pick(v, self.xs)))
+        for k in ("master", "m", "v"):
+            assert np.array_equal(bits32(got[k]), bits32(want[k])), k
+        assert np.array_equal(got["shards"], want["shards"])
+
+    def check_gather(self, full):
+        """The gathered buffer holds the pre-step bf16 shard values."""
+        got = u16(pick(full, self.e[self.valid]))
+        assert np.array_equal(got, self.shards[self.valid])
+
+
+def _layer_step(z3mod, orc, w, seed):
+    dev = torch.device("cuda")
+    L = z3mod.Layout(w.numel, w.n_ranks)
+    O = orc.layout(w.numel, w.n_ranks)
+    gen = I.make_generator(seed, dev)
+    full32 = I.draw_master(w, gen, dev)
+    T = L.psi_padded
+    shards = torch.empty(T, dtype=torch.bfloat16, device=dev)
+    master, m, v = (torch.empty(T, dtype=torch.float32, device=dev) for _ in range(3))
+    z3mod.z3_partition(L, full32, shards, master, m, v)
+    # partition at the sampled positions
+    pr = Probe(orc, O, shards, master, m, v)
+    ev = pr.e[pr.valid]
+    assert np.array_equal(bits32(pr.master[pr.valid]), bits32(f32(pick(full32, ev))))
+    assert not pr.master[~pr.valid].any() and not pr.shards[~pr.valid].any()
+    del full32
+    full = torch.empty(L.psi, dtype=torch.bfloat16, device=dev)
+    for t in (1, 2):
+        grads = I.draw_grads(w, gen, dev)
+        pr = Probe(orc, O, shards, master, m, v, seed=t)
+        want = pr.expected(orc, grads, w.grad_stride, 1.0 / w.n_ranks, w.hp, t)
+        z3mod.z3_step_layer(L, shards, full, grads, w.grad_stride, 1.0 / w.n_ranks, master, m,
+                            v, w.hp, t)
+        torch.cuda.synchronize()
+        pr.check_gather(full)
+        pr.check_after(want, shards, master, m, v)
+        del grads
+
+
+@pytest.mark.parametrize("n_ranks", [8, 64])
+def test_layer_7b(z3mod, orc, n_ranks):
+    _layer_step(z3mod, orc, I.layer_7b(n_ranks), seed=7)
+
+
+def test_full_step_24_layers(z3mod, orc):
+    """24 d=1024 layers + embedding, N_d = 16: forward gathers of every unit,
+    then backward gather + fused reduce-scatter/Adam in reverse unit order,
+    all through one transient buffer."""
+    from optimizer_state_gb300 import schedule
+    dev = torch.device("cuda")
+    model = schedule.full_step_model(dev, seed=3)
+    assert model.psi == 353502208
+    assert model.full.numel() == 50257 * 1024          # the largest unit
+    probes = []
+    for u in model.units:
+        O = orc.layout(u.w.numel, u.w.n_ranks)
+        probes.append(Probe(orc, O, u.shards, u.master, u.m, u.v, n_random=1 << 15))
+    wants = [pr.expected(orc, u.grads, u.w.grad_stride, 1.0 / u.w.n_ranks, HP, 1)
+             for pr, u in zip(probes, model.units)]
+    watch = {("forward", 0), ("forward", 1), ("forward", 24), ("backward", 24),
+             ("backward", 1), ("backward", 0)}
+    snaps = {}
+
+    def on_gather(phase, i):
+        if (phase, i) in watch:
+            snaps[(phase, i)] = model.full[:model.units[i].L.psi].clone()
+    model.step(HP, on_gather=on_gather)
+    torch.cuda.synchronize()
+    for (phase, i), buf in snaps.items():
+        probes[i].check_gather(buf)          # every gather saw pre-step shards
+    for pr, want, u in zip(probes, wants, model.units):
+        pr.check_after(want, u.shards, u.master, u.m, u.v)
+
+
+def _sweep_point(z3mod, orc, n, n_ranks, full_check: bool, seed=5):
+    """One step of the sweep workload: forward and backward gathers, then 4
+    micro-batches reduce-scattered and accumulated into fp32 slices, the last
+    one fused with Adam ('ZeRO Stages: ...', stage-2 accumulation)."""
+    w = I.sweep(n, n_ranks)
+    dev = torch.device("cuda")
+    L = z3mod.Layout(w.numel, n_ranks)
+    O = orc.layout(w.numel, n_ranks)
+    gen = I.make_generator(seed, dev)
+    full32 = I.draw_master(w, gen, dev)
+    T, stride, scale = L.psi_padded, w.grad_stride, 1.0 / n_ranks
+    shards = torch.empty(T, dtype=torch.bfloat16, device=dev)
+    master, m, v, acc = (torch.empty(T, dtype=torch.float32, device=dev) for _ in range(4))
+    full = torch.empty(L.psi, dtype=torch.bfloat16, device=dev)
+    z3mod.z3_partition(L, full32, shards, master, m, v)
+    if full_check:
+        o_sh, o_ma, o_m, o_v = orc.partition(O, f32(full32))
+        assert np.array_equal(u16(shards), o_sh) and np.array_equal(bits32(f32(master)),
+                                                                    bits32(o_ma))
+    del full32
+    pr = None if full_check else Probe(orc, O, shards, master, m, v, n_random=1 << 20)
+    z3mod.z3_allgather(L, shards, full)
+    z3mod.z3_allgather(L, shards, full)
+    grads = torch.zeros((n_ranks, stride), dtype=torch.bfloat16, device=dev)
+    o_acc = None
+    p_acc = None
+    for mb in range(w.micro_batches):
+        I.draw_grads(w, gen, dev, out=grads)
+        last = mb == w.micro_batches - 1
+        if full_check:
+            gh = u16(grads).reshape(-1)
+            if mb == 0:
+                o_acc = orc.reduce_scatter(O, gh, stride, scale)
+            elif not last:
+                orc.reduce_scatter(O, gh, stride, scale, out=o_acc, accumulate=True)
+            else:
+                want_full = orc.allgather(O, o_sh)
+                orc.step_layer(O, o_sh, gh, stride, scale, o_ma, o_m, o_v, w.hp, 1,
+                               grad_acc=o_acc.copy())
+        else:
+            ev = pr.e[pr.valid]
+            G = np.ascontiguousarray(gather_rows(grads, n_ranks, stride, ev))
+            fold = orc.allreduce(orc.layout([int(ev.size)], n_ranks), G.reshape(-1),
+                                 int(ev.size), scale)
+            if mb == 0:
+                p_acc = np.zeros(pr.xs.size, np.float32)
+                p_acc[pr.valid] = fold
+            elif not last:
+                p_acc[pr.valid] = (p_acc[pr.valid] + fold).astype(np.float32)
+            else:
+                want = pr.expected(orc, grads, stride, scale, w.hp, 1, acc=p_acc)
+        if mb == 0:
+            z3mod.z3_reduce_scatter(L, grads, stride, acc, scale)
+        elif not last:
+            z3mod.z3_reduce_scatter(L, grads, stride, acc, scale, accumulate=True)
+        else:
+            z3mod.z3_reduce_scatter_adam(L, grads, stride, scale, acc, master, m, v, shards,
+                                         w.hp, 1)
+    torch.cuda.synchronize()
+    if full_check:
+        assert np.array_equal(u16(full), want_full)
+        assert np.array_equal(bits32(f32(acc)), bits32(o_acc))
+        assert np.array_equal(bits32(f32(master)), bits32(o_ma))
+        assert np.array_equal(bits32(f32(m)), bits32(o_m))
+        assert np.array_equal(bits32(f32(v)), bits32(o_v))
+        assert np.array_equal(u16(shards), o_sh)
+    else:
+        pr.check_gather(full)
+        assert np.array_equal(bits32(f32(pick(acc, pr.xs))), bits32(p_acc))
+        pr.check_after(want, shards, master, m, v)
+
+
+@pytest.mark.parametrize("n_ranks", [2, 8, 64])
+@pytest.mark.parametrize("n", [262147, 4194319])
+def test_sweep_full_check(z3mod, orc, n, n_ranks):
+    _sweep_point(z3mod, orc, n, n_ranks, full_check=True)
+
+
+@pytest.mark.parametrize("n,n_ranks", [(67108879, 8), (2 ** 31 - 1, 2), (2 ** 31 - 1, 8),
+                                       (1073741827, 64)])
+def test_sweep_largest_points_sampled(z3mod, orc, n, n_ranks):
+    """The largest sweep points that fit HBM (2^30+3 at N_d = 64 reads a
+    137 GB gradient buffer; 2^31-1 at N_d = 64 would need 275 GB and is the
+    capacity cap)."""
+    _sweep_point(z3mod, orc, n, n_ranks, full_check=False)
