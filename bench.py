@@ -198,7 +198,7 @@ def run_cuda(args, world, rank, local):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    w = I.LAYER_D1024
+    w = layer_workload(args.workload)
     L = z3.Layout(w.numel, w.n_ranks)
     stats = L.stats()
     step_bytes = stats["hbm_step_layer"]
@@ -270,7 +270,7 @@ def run_cuda(args, world, rank, local):
         peak, peak_kind = measured_hbm_peak()
         rs_bytes = stats["hbm_reduce_scatter_adam"]
         achieved = rs_bytes / (t_rs * 1e-3) / 1e9
-        traffic = profiled_traffic("k_reduce_rs_adam", "layer_d1024_nd8")
+        traffic = profiled_traffic("k_reduce_rs_adam", args.workload)
         line = {
             "metric": METRIC,
             "value": round(value, 2),
@@ -285,9 +285,8 @@ def run_cuda(args, world, rank, local):
             "dtype": "f32",
             "data": "synthetic",
             "config": {
-                "workload": "layer_d1024_nd8",
-                "layer": "d_model=1024: Wqkv[3072,1024] Wo[1024,1024] W_up[4096,1024] "
-                         "W_down[1024,4096] 2x norm[1024]",
+                "workload": args.workload,
+                "layer": " ".join("x".join(map(str, sh)) for sh in w.shapes),
                 "psi": L.psi, "n_ranks": w.n_ranks, "S": L.S,
                 "storage": "bf16 params/grads, fp32 master/m/v",
                 "bytes_per_param": 2 * w.n_ranks + 34,
@@ -322,10 +321,97 @@ def run_cuda(args, world, rank, local):
         dist.destroy_process_group()
 
 
+LAYER_WORKLOADS = ("layer_d1024_nd8", "layer_7b_nd8", "layer_7b_nd64")
+
+
+def layer_workload(name: str):
+    from optimizer_state_gb300 import inputs as I
+    if name == "layer_d1024_nd8":
+        return I.LAYER_D1024
+    if name.startswith("layer_7b_nd"):
+        return I.layer_7b(int(name[len("layer_7b_nd"):]))
+    raise SystemExit(f"unknown layer workload {name}")
+
+
 def len_tabs(L, kind):
     """Launches per call: one per launch table (a table holds <= 40 params)."""
     n = sum(1 for x in L.numel if x > 0)
     return -(-n // 40)
+
+
+def run_multi(args, world, rank, local):
+    """Full step (24 layers + embedding, N_d = 16) or one sweep point
+    (AG, AG, 4 micro-batches reduced and accumulated, Adam fused with the
+    last): the step is timed as a whole with CUDA events."""
+    import torch
+    from optimizer_state_gb300 import build as libbuild
+    from optimizer_state_gb300 import inputs as I
+    from optimizer_state_gb300 import schedule, z3
+    libbuild.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream()
+    sid = stream.cuda_stream
+    if args.workload == "full_step_nd16":
+        model = schedule.full_step_model(dev, seed=rank)
+        step_bytes, psi, launches = model.step_bytes, model.psi, model.launches_per_step()
+
+        def step(i):
+            model.step(HP, stream=sid)
+        extra = {"units": len(model.units), "n_ranks": 16,
+                 "bytes_per_param": 66, "transient_buffer_elems": model.full.numel()}
+    elif args.workload.startswith("sweep_n"):
+        n_s, nd_s = args.workload[len("sweep_n"):].split("_nd")
+        w = I.sweep(int(n_s), int(nd_s))
+        u = schedule.Unit(w, dev, I.make_generator(rank, dev))
+        full = torch.empty(u.L.psi, dtype=torch.bfloat16, device=dev)
+        acc = torch.empty(u.L.psi_padded, dtype=torch.float32, device=dev)
+        st = u.L.stats()
+        step_bytes = 2 * st["hbm_allgather"] + st["hbm_reduce_scatter"] + \
+            (w.micro_batches - 2) * st["hbm_reduce_scatter_accumulate"] + \
+            st["hbm_reduce_scatter_adam"] + 4 * u.L.psi
+        psi, launches = u.L.psi, 2 + w.micro_batches
+        scale = 1.0 / w.n_ranks
+
+        def step(i):
+            z3.z3_allgather(u.L, u.shards, full, stream=sid)
+            z3.z3_allgather(u.L, u.shards, full, stream=sid)
+            z3.z3_reduce_scatter(u.L, u.grads, w.grad_stride, acc, scale, stream=sid)
+            for _ in range(w.micro_batches - 2):
+                z3.z3_reduce_scatter(u.L, u.grads, w.grad_stride, acc, scale, accumulate=True,
+                                     stream=sid)
+            z3.z3_reduce_scatter_adam(u.L, u.grads, w.grad_stride, scale, acc, u.master, u.m,
+                                      u.v, u.shards, HP, i + 1, stream=sid)
+        extra = {"n": w.numel[0], "n_ranks": w.n_ranks, "micro_batches": w.micro_batches,
+                 "note": "one gradient buffer re-read by every micro-batch"}
+    else:
+        raise SystemExit(f"unknown workload {args.workload}")
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_max = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    value = aggregate_gbs(world, step_bytes, args.steps, ms_max)
+    if rank == 0:
+        peak, kind = measured_hbm_peak()
+        print(json.dumps({
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_max / args.steps, 6), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": dict(workload=args.workload, psi=psi, step_bytes=step_bytes, **extra),
+            "params_per_s": round(world * psi * args.steps / (ms_max * 1e-3), 1),
+            "pct_of_8tbs": round(100.0 * value / (NOMINAL_HBM_GBS * world), 2),
+            "frac_of_measured_peak": round(value / world / peak, 4), "peak_kind": kind,
+            "gpu_launches": launches * args.steps}), flush=True)
 
 
 def run_e2e(args, z3, L, w, rep, stream, sid, step_bytes, world):
@@ -466,6 +552,9 @@ def main():
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="layer_d1024_nd8",
+                    help="layer_d1024_nd8 (default), layer_7b_nd8, layer_7b_nd64, "
+                         "full_step_nd16, or sweep_n<N>_nd<R>")
     ap.add_argument("--kernel-steps", type=int, default=500)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cold-bytes", type=int, default=1536 << 20,
@@ -482,8 +571,10 @@ def main():
             sys.exit("--gpus N > 1 must be launched with torchrun (one process per GPU)")
     if args.impl == "reference":
         run_reference(args, world, rank)
-    else:
+    elif args.workload in LAYER_WORKLOADS:
         run_cuda(args, world, rank, local)
+    else:
+        run_multi(args, world, rank, local)
 
 
 if __name__ == "__main__":
