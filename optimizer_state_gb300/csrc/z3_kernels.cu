@@ -132,6 +132,17 @@ __device__ __forceinline__ TileRef locate(const Tab &tab, int64_t g) {
     return TileRef{lo, r, local - r * tpc};
 }
 
+// Programmatic dependent launch.  Every kernel lets the next kernel of the
+// stream launch at once (its CTAs then wait), and waits for the previous
+// kernel to complete -- memory included -- before its first global memory
+// access.  Ordering between the calls is therefore exactly stream order; only
+// the launch latency of a kernel overlaps the tail of the one before it.
+// Without the launch attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // --------------------------------------------------------------------------
 // AllGather: full[F_p + i] = shards[i / s_p][o_p + i mod s_p]
 // --------------------------------------------------------------------------
@@ -182,6 +193,7 @@ __device__ __forceinline__ void gather_tile(const Tab &tab, const GatherArgs &a,
 template <bool ALIGNED>
 __global__ void __launch_bounds__(kGatherThreads)
 k_allgather(const __grid_constant__ Tab tab, const GatherArgs a) {
+    pdl_enter();
     const TileRef tr = locate(tab, blockIdx.x);
     const TabEntry &e = tab.e[tr.p];
     const int64_t d0 = e.F + tr.r * e.s;
@@ -371,6 +383,7 @@ __device__ __forceinline__ void reduce_tile(const ReduceArgs &a, int n_ranks, in
 template <bool ALIGNED, int MODE>
 __global__ void __launch_bounds__(kReduceThreads)
 k_reduce(const __grid_constant__ Tab tab, const ReduceArgs a) {
+    pdl_enter();
     const TileRef tr = locate(tab, blockIdx.x);
     const TabEntry &e = tab.e[tr.p];
     const int64_t c0 = tr.r * tab.S + e.o;
@@ -436,6 +449,7 @@ template <int MODE>
 __global__ void __launch_bounds__(kReduceThreads, 4)
 k_reduce_aligned(const __grid_constant__ Tab tab, const ReduceArgs a) {
     static_assert(kReduceVecPerThread == 1, "one vector per thread");
+    pdl_enter();
     const TileRef tr = locate(tab, blockIdx.x);
     const TabEntry &e = tab.e[tr.p];
     const int64_t c0 = tr.r * tab.S + e.o;
@@ -464,6 +478,7 @@ struct PartitionArgs {
 
 __global__ void __launch_bounds__(kReduceThreads)
 k_partition(const __grid_constant__ Tab tab, const PartitionArgs a) {
+    pdl_enter();
     const TileRef tr = locate(tab, blockIdx.x);
     const TabEntry &e = tab.e[tr.p];
     const int64_t c0 = tr.r * tab.S + e.o;
@@ -498,6 +513,7 @@ struct AdamArgs {
 constexpr int kAdamThreads = 256;
 
 __global__ void __launch_bounds__(kAdamThreads) k_adam(const AdamArgs a) {
+    pdl_enter();
     const int64_t x0 = ((int64_t)blockIdx.x * kAdamThreads + threadIdx.x) * kVec;
     if (x0 >= a.total) return;
     if (x0 + kVec <= a.total) {
@@ -600,15 +616,32 @@ z3_status launched(const char *fn) {
     return Z3_OK;
 }
 
+// Launches a kernel with programmatic stream serialisation allowed.
+template <typename... KArgs, typename... Args>
+void launch(void (*kernel)(KArgs...), int64_t grid, int block, cudaStream_t stream,
+            Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    (void)cudaLaunchKernelEx(&cfg, kernel, args...);  // errors: cudaGetLastError in launched()
+}
+
 // Enqueue helpers (no validation).
 z3_status run_allgather(const z3_layout *L, const uint16_t *shards, uint16_t *full,
                         cudaStream_t stream) {
     const GatherArgs a{shards, full};
     for (const Tab &t : L->gather_tabs) {
         if (t.phase0)
-            k_allgather<true><<<(unsigned)t.tiles, kGatherThreads, 0, stream>>>(t, a);
+            launch(k_allgather<true>, t.tiles, kGatherThreads, stream, t, a);
         else
-            k_allgather<false><<<(unsigned)t.tiles, kGatherThreads, 0, stream>>>(t, a);
+            launch(k_allgather<false>, t.tiles, kGatherThreads, stream, t, a);
     }
     return launched("z3_allgather");
 }
@@ -616,9 +649,9 @@ z3_status run_allgather(const z3_layout *L, const uint16_t *shards, uint16_t *fu
 template <int MODE>
 z3_status launch_reduce(const Tab &t, const ReduceArgs &a, cudaStream_t stream) {
     if (t.phase0)
-        k_reduce_aligned<MODE><<<(unsigned)t.tiles, kReduceThreads, 0, stream>>>(t, a);
+        launch(k_reduce_aligned<MODE>, t.tiles, kReduceThreads, stream, t, a);
     else
-        k_reduce<false, MODE><<<(unsigned)t.tiles, kReduceThreads, 0, stream>>>(t, a);
+        launch(k_reduce<false, MODE>, t.tiles, kReduceThreads, stream, t, a);
     return Z3_OK;
 }
 
@@ -654,7 +687,7 @@ extern "C" z3_status z3_partition(const z3_layout *L, const float *full, uint16_
     if (T == 0) return Z3_OK;
     const PartitionArgs a{full, shards, master, m, v};
     for (const Tab &t : L->reduce_tabs)
-        k_partition<<<(unsigned)t.tiles, kReduceThreads, 0, (cudaStream_t)stream>>>(t, a);
+        launch(k_partition, t.tiles, kReduceThreads, (cudaStream_t)stream, t, a);
     return launched(fn);
 }
 
@@ -713,7 +746,7 @@ extern "C" z3_status z3_adam_shard_step(const z3_layout *L, float *master, float
     a.total = T;
     const int64_t blocks = (T + (int64_t)kAdamThreads * kVec - 1) / ((int64_t)kAdamThreads * kVec);
     if (blocks > 0x7fffffff) return fail(Z3_ERR_OVERFLOW, "z3_adam_shard_step: grid too large");
-    k_adam<<<(unsigned)blocks, kAdamThreads, 0, (cudaStream_t)stream>>>(a);
+    launch(k_adam, blocks, kAdamThreads, (cudaStream_t)stream, a);
     return launched(fn);
 }
 
