@@ -195,6 +195,27 @@ z3_status z3_step_layer(const z3_layout *layout, uint16_t *shards,
                         float *m, float *v, const z3_adam_hp *hp,
                         int64_t step, z3_stream stream);
 
+/* ---- stage 1 / stage 2 / plain data-parallel variants ------------------ */
+
+/* Plain data-parallel all-reduce ([S3] communication list: the baseline's
+ * one all-reduce; [ZS] "Stage 2 also partitions gradients": an all-reduce is
+ * a reduce-scatter followed by an all-gather).  Writes the one replica of the
+ * reduced gradient that every rank would hold:
+ *   out[e] = scale * fold_k fp32(grads[k][e]), 0 <= e < Psi,
+ * with the rank fold of z3_reduce_scatter (ascending rank order, binary32).
+ * grads is read; out (fp32 [Psi]) is written. */
+z3_status z3_allreduce(const z3_layout *layout, const uint16_t *grads,
+                       int64_t grad_stride, float *out, float scale,
+                       z3_stream stream);
+
+/* The slice of a replicated fp32 tensor that each rank keeps ([ZS] "What
+ * stage 1 partitions": each rank applies the optimiser only to its own slice
+ * of the gradient it received):
+ *   shards[r][o_p + j] = full[F_p + r*s_p + j] for r*s_p + j < n_p, 0 in the
+ * pad.  full (fp32 [Psi]) is read; shards (fp32 [N][S]) is written. */
+z3_status z3_scatter(const z3_layout *layout, const float *full, float *shards,
+                     z3_stream stream);
+
 /* ---- errors ------------------------------------------------------------ */
 
 /* Static name of a status code. */

@@ -546,6 +546,85 @@ __global__ void __launch_bounds__(kAdamThreads) k_adam(const AdamArgs a) {
 }
 
 // --------------------------------------------------------------------------
+// Plain data-parallel all-reduce into one fp32 replica, and the scatter of a
+// replicated fp32 tensor into the [N][S] shard layout (stage-1 variant)
+// --------------------------------------------------------------------------
+
+struct AllreduceArgs {
+    const uint16_t *__restrict__ grads;
+    int64_t stride;
+    float *__restrict__ out;
+    int64_t psi;
+    float scale;
+    int n_ranks;
+};
+
+constexpr int kFlatThreads = 256;
+
+// One vector of 8 full-space elements per thread: grads rows start on
+// 16-byte boundaries (stride is a multiple of 8), so every vector is aligned.
+__global__ void __launch_bounds__(kFlatThreads, 4) k_allreduce(const AllreduceArgs a) {
+    pdl_enter();
+    const int64_t x0 = ((int64_t)blockIdx.x * kFlatThreads + threadIdx.x) * kVec;
+    if (x0 >= a.psi) return;
+    if (x0 + kVec <= a.psi) {
+        const uint16_t *gp = a.grads + x0;
+        float acc[8];
+        for (int k0 = 0; k0 < a.n_ranks; k0 += kRankBatch) {
+            uint4 w[kRankBatch];
+#pragma unroll
+            for (int u = 0; u < kRankBatch; ++u)
+                if (k0 + u < a.n_ranks) w[u] = ld_nc(gp + (int64_t)(k0 + u) * a.stride);
+#pragma unroll
+            for (int u = 0; u < kRankBatch; ++u) {
+                if (k0 + u < a.n_ranks) {
+                    float f[8];
+                    unpack8(w[u], f);
+                    if (k0 + u == 0) {
+#pragma unroll
+                        for (int l = 0; l < 8; ++l) acc[l] = f[l];
+                    } else {
+#pragma unroll
+                        for (int l = 0; l < 8; ++l) acc[l] = __fadd_rn(acc[l], f[l]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int l = 0; l < 8; ++l) acc[l] = __fmul_rn(acc[l], a.scale);
+        st8f(a.out + x0, acc);
+    } else {
+        for (int64_t e = x0; e < a.psi; ++e) {
+            float s = bf16_to_f32(a.grads[e]);
+            for (int k = 1; k < a.n_ranks; ++k)
+                s = __fadd_rn(s, bf16_to_f32(a.grads[(int64_t)k * a.stride + e]));
+            a.out[e] = __fmul_rn(s, a.scale);
+        }
+    }
+}
+
+struct ScatterArgs {
+    const float *__restrict__ full;
+    float *__restrict__ shards;
+};
+
+// Element-wise over each reduce tile (coalesced 4-byte accesses).
+__global__ void __launch_bounds__(kReduceThreads) k_scatter(const __grid_constant__ Tab tab,
+                                                            const ScatterArgs a) {
+    pdl_enter();
+    const TileRef tr = locate(tab, blockIdx.x);
+    const TabEntry &e = tab.e[tr.p];
+    const int64_t c0 = tr.r * tab.S + e.o;
+    const int64_t c_end = c0 + e.s;
+    const int64_t valid_end = c0 + min(e.s, max((int64_t)0, e.n - tr.r * e.s));
+    const int64_t delta = e.F + tr.r * e.s - c0;
+    const int64_t x_beg = (c0 / kVec + tr.t * (int64_t)(kReduceThreads * kReduceVecPerThread)) * kVec;
+    const int64_t x_end = min(c_end, x_beg + (int64_t)(kReduceThreads * kReduceVecPerThread) * kVec);
+    for (int64_t x = max(x_beg, c0) + threadIdx.x; x < x_end; x += kReduceThreads)
+        a.shards[x] = x < valid_end ? a.full[x + delta] : 0.0f;
+}
+
+// --------------------------------------------------------------------------
 // host-side validation helpers
 // --------------------------------------------------------------------------
 
@@ -815,4 +894,36 @@ extern "C" z3_status z3_step_layer(const z3_layout *L, uint16_t *shards, uint16_
     st = run_allgather(L, shards, full, s);
     if (st != Z3_OK) return st;
     return run_reduce(L, a, kRSAdam, s, fn);
+}
+
+extern "C" z3_status z3_allreduce(const z3_layout *L, const uint16_t *grads, int64_t grad_stride,
+                                  float *out, float scale, z3_stream stream) {
+    const char *fn = "z3_allreduce";
+    if (L == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_allreduce: layout is NULL");
+    if (!std::isfinite(scale)) return fail(Z3_ERR_INVALID_ARG, "z3_allreduce: scale");
+    int64_t gbytes;
+    z3_status st = check_grads(fn, L, grad_stride, &gbytes);
+    if (st != Z3_OK) return st;
+    const Buf bufs[2] = {{grads, L->psi ? gbytes : 0, "grads"}, {out, 4 * L->psi, "out"}};
+    st = check_bufs(fn, bufs, 2);
+    if (st != Z3_OK) return st;
+    if (L->psi == 0) return Z3_OK;
+    const int64_t blocks = (L->psi + (int64_t)kFlatThreads * kVec - 1) / ((int64_t)kFlatThreads * kVec);
+    if (blocks > 0x7fffffff) return fail(Z3_ERR_OVERFLOW, "z3_allreduce: grid too large");
+    const AllreduceArgs a{grads, grad_stride, out, L->psi, scale, L->n_ranks};
+    launch(k_allreduce, blocks, kFlatThreads, (cudaStream_t)stream, a);
+    return launched(fn);
+}
+
+extern "C" z3_status z3_scatter(const z3_layout *L, const float *full, float *shards,
+                                z3_stream stream) {
+    const char *fn = "z3_scatter";
+    if (L == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_scatter: layout is NULL");
+    const Buf bufs[2] = {{full, 4 * L->psi, "full"}, {shards, 4 * L->psi_padded, "shards"}};
+    z3_status st = check_bufs(fn, bufs, 2);
+    if (st != Z3_OK) return st;
+    if (L->psi_padded == 0) return Z3_OK;
+    const ScatterArgs a{full, shards};
+    for (const Tab &t : L->reduce_tabs) launch(k_scatter, t.tiles, kReduceThreads, (cudaStream_t)stream, t, a);
+    return launched(fn);
 }

@@ -93,3 +93,60 @@ def full_step_model(dev, seed: int = 0) -> Model:
     gen = I.make_generator(seed, dev)
     return Model([Unit(w, dev, gen) for w in I.full_step_units()], dev)
 
+
+
+# ---------------------------------------------------------------------------
+# The other ZeRO stages and plain data parallelism on the same kernels
+# ("ZeRO Stages: Sharding Optimizer State, Gradients, and Parameters";
+# "ZeRO Stage 3: Parameter Partitioning", communication list).  Each returns
+# the HBM bytes per unpadded element its launches move.
+# ---------------------------------------------------------------------------
+
+def stage2_step(u: Unit, full: torch.Tensor, hp: dict, t: int, stream=None) -> int:
+    """Stage 2: reduce-scatter the gradients (fused with the shard Adam), then
+    one all-gather of the updated parameters into the replica."""
+    N = u.w.n_ranks
+    z3.z3_reduce_scatter_adam(u.L, u.grads, u.w.grad_stride, 1.0 / N, None, u.master, u.m, u.v,
+                              u.shards, hp, t, stream=stream)
+    z3.z3_allgather(u.L, u.shards, full, stream=stream)
+    return (2 * N + 26) + 4
+
+
+def stage1_step(u: Unit, grad_full: torch.Tensor, grad_shards: torch.Tensor,
+                full: torch.Tensor, hp: dict, t: int, stream=None) -> int:
+    """Stage 1: all-reduce the gradients (every rank receives the full sum),
+    each rank updates its slice of the optimizer state from its slice of the
+    reduced gradient, then an all-gather of the updated parameters."""
+    N = u.w.n_ranks
+    z3.z3_allreduce(u.L, u.grads, u.w.grad_stride, grad_full, 1.0 / N, stream=stream)
+    z3.z3_scatter(u.L, grad_full, grad_shards, stream=stream)
+    z3.z3_adam_shard_step(u.L, u.master, u.m, u.v, grad_shards, u.shards, hp, t, stream=stream)
+    z3.z3_allgather(u.L, u.shards, full, stream=stream)
+    return (2 * N + 4) + 8 + 30 + 4
+
+
+class DPReplica:
+    """Plain data parallelism: every rank holds the whole fp32 master, m, v and
+    bf16 parameters; the state is laid out as one rank (N = 1)."""
+
+    def __init__(self, w: I.Workload, dev, gen: torch.Generator):
+        self.w = w
+        self.L = z3.Layout(w.numel, w.n_ranks)         # the gradient fold over N ranks
+        self.L1 = z3.Layout(w.numel, 1)                # unsharded state
+        n = self.L1.psi
+        self.params = torch.empty(n, dtype=torch.bfloat16, device=dev)
+        self.master = torch.empty(n, dtype=torch.float32, device=dev)
+        self.m = torch.empty(n, dtype=torch.float32, device=dev)
+        self.v = torch.empty(n, dtype=torch.float32, device=dev)
+        full = I.draw_master(w, gen, dev).to(dev)
+        z3.z3_partition(self.L1, full, self.params, self.master, self.m, self.v)
+        self.grads = I.draw_grads(w, gen, dev).to(dev)
+        self.grad_full = torch.empty(n, dtype=torch.float32, device=dev)
+
+    def step(self, hp: dict, t: int, stream=None) -> int:
+        N = self.w.n_ranks
+        z3.z3_allreduce(self.L, self.grads, self.w.grad_stride, self.grad_full, 1.0 / N,
+                        stream=stream)
+        z3.z3_adam_shard_step(self.L1, self.master, self.m, self.v, self.grad_full, self.params,
+                              hp, t, stream=stream)
+        return (2 * N + 4) + 30

@@ -25,6 +25,7 @@ Z3_OK, Z3_ERR_INVALID_ARG, Z3_ERR_ALIGNMENT, Z3_ERR_OVERFLOW, Z3_ERR_CUDA = rang
 EXPORTS = ("z3_layout_create", "z3_layout_destroy", "z3_layout_info", "z3_layout_params",
            "z3_stats", "z3_partition", "z3_allgather", "z3_reduce_scatter",
            "z3_adam_shard_step", "z3_reduce_scatter_adam", "z3_step_layer",
+           "z3_allreduce", "z3_scatter",
            "z3_status_string", "z3_last_error")
 
 
@@ -81,6 +82,8 @@ def load():
             "z3_adam_shard_step": (st, [vp, vp, vp, vp, vp, vp, hp, i64, vp]),
             "z3_reduce_scatter_adam": (st, [vp, vp, i64, f32, vp, vp, vp, vp, vp, hp, i64, vp]),
             "z3_step_layer": (st, [vp, vp, vp, vp, i64, f32, vp, vp, vp, hp, i64, vp]),
+            "z3_allreduce": (st, [vp, vp, i64, vp, f32, vp]),
+            "z3_scatter": (st, [vp, vp, vp, vp]),
             "z3_status_string": (ctypes.c_char_p, [st]),
             "z3_last_error": (ctypes.c_size_t, [ctypes.c_char_p, ctypes.c_size_t]),
         }
@@ -248,3 +251,16 @@ def z3_step_layer(layout: Layout, shards, full, grads, grad_stride: int, scale: 
         _dev(grads, b16, layout.n_ranks * grad_stride, "grads"), grad_stride, scale,
         _dev(master, f32, T, "master"), _dev(m, f32, T, "m"), _dev(v, f32, T, "v"),
         ctypes.byref(h), step, _stream(stream)))
+
+
+def z3_allreduce(layout: Layout, grads, grad_stride: int, out, scale: float, stream=None):
+    b16, f32 = _dtypes()
+    _check(load().z3_allreduce(
+        layout.handle, _dev(grads, b16, layout.n_ranks * grad_stride, "grads"), grad_stride,
+        _dev(out, f32, layout.psi, "out"), scale, _stream(stream)))
+
+
+def z3_scatter(layout: Layout, full, shards, stream=None):
+    _, f32 = _dtypes()
+    _check(load().z3_scatter(layout.handle, _dev(full, f32, layout.psi, "full"),
+                             _dev(shards, f32, layout.psi_padded, "shards"), _stream(stream)))
