@@ -387,6 +387,39 @@ def run_multi(args, world, rank, local):
                                       u.v, u.shards, HP, i + 1, stream=sid)
         extra = {"n": w.numel[0], "n_ranks": w.n_ranks, "micro_batches": w.micro_batches,
                  "note": "one gradient buffer re-read by every micro-batch"}
+    elif args.workload in ("dp_d1024_nd8", "stage1_d1024_nd8", "stage2_d1024_nd8"):
+        w = I.LAYER_D1024
+        kind = args.workload.split("_")[0]
+        n_rep = 4                                   # rotating replicas: every step cold
+        if kind == "dp":
+            reps = [schedule.DPReplica(w, dev, I.make_generator(100 * rank + i, dev))
+                    for i in range(n_rep)]
+            bpp = (2 * w.n_ranks + 4) + 30
+
+            def step(i):
+                reps[i % n_rep].step(HP, i + 1, stream=sid)
+        else:
+            reps = [schedule.Unit(w, dev, I.make_generator(100 * rank + i, dev))
+                    for i in range(n_rep)]
+            L0 = reps[0].L
+            full = torch.empty(L0.psi, dtype=torch.bfloat16, device=dev)
+            gfull = torch.empty(L0.psi, dtype=torch.float32, device=dev)
+            gsh = torch.empty(L0.psi_padded, dtype=torch.float32, device=dev)
+            if kind == "stage1":
+                bpp = (2 * w.n_ranks + 4) + 8 + 30 + 4
+
+                def step(i):
+                    schedule.stage1_step(reps[i % n_rep], gfull, gsh, full, HP, i + 1, stream=sid)
+            else:
+                bpp = (2 * w.n_ranks + 26) + 4
+
+                def step(i):
+                    schedule.stage2_step(reps[i % n_rep], full, HP, i + 1, stream=sid)
+        psi = w.psi
+        step_bytes = bpp * psi
+        launches = {"dp": 2, "stage1": 4, "stage2": 2}[kind]
+        extra = {"n_ranks": w.n_ranks, "bytes_per_param": bpp, "variant": kind,
+                 "l2": f"{n_rep} rotating replicas"}
     else:
         raise SystemExit(f"unknown workload {args.workload}")
     for i in range(args.warmup):
