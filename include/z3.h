@@ -216,6 +216,22 @@ z3_status z3_allreduce(const z3_layout *layout, const uint16_t *grads,
 z3_status z3_scatter(const z3_layout *layout, const float *full, float *shards,
                      z3_stream stream);
 
+/* ---- checkpoint resharding --------------------------------------------- */
+
+/* Re-lays one [N][S] state buffer of a layer from src_layout's rank count to
+ * dst_layout's ([ZS] "Where the shards live and what happens on failure":
+ * loading a per-rank shard set at a different P needs a reshuffle, not a
+ * file copy).  Both layouts must describe the same parameters (same n_p, in
+ * order).  For every destination position with padded index i = r'*s'_p + j'
+ * < n_p: dst[r'][o'_p + j'] = src[i / s_p][o_p + i mod s_p]; pad positions
+ * get 0.  elem_bytes is 2 (bf16 shards) or 4 (fp32 master, m, v, gradient
+ * shards).  src is read, dst written; they must not overlap.  Errors:
+ * different parameter lists (INVALID_ARG), elem_bytes not 2 or 4
+ * (INVALID_ARG), and the usual buffer checks. */
+z3_status z3_reshard(const z3_layout *src_layout, const z3_layout *dst_layout,
+                     int32_t elem_bytes, const void *src, void *dst,
+                     z3_stream stream);
+
 /* ---- errors ------------------------------------------------------------ */
 
 /* Static name of a status code. */

@@ -34,6 +34,7 @@
 #include <cmath>
 #include <cstdint>
 #include <string>
+#include <vector>
 
 #include "z3_internal.h"
 
@@ -625,6 +626,43 @@ __global__ void __launch_bounds__(kReduceThreads) k_scatter(const __grid_constan
 }
 
 // --------------------------------------------------------------------------
+// Reshard: one [N][S] buffer to another rank count (checkpoint loading)
+// --------------------------------------------------------------------------
+
+// Source-layout facts of the parameters of one destination launch table,
+// entry for entry.
+struct SrcTab {
+    int64_t S;
+    int64_t s[kTabMax];
+    int64_t o[kTabMax];
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kReduceThreads)
+k_reshard(const __grid_constant__ Tab tab, const __grid_constant__ SrcTab src_tab,
+          const T *__restrict__ src, T *__restrict__ dst) {
+    pdl_enter();
+    const TileRef tr = locate(tab, blockIdx.x);
+    const TabEntry &e = tab.e[tr.p];
+    const int64_t s_src = src_tab.s[tr.p];
+    const int64_t o_src = src_tab.o[tr.p];
+    const int64_t c0 = tr.r * tab.S + e.o;
+    const int64_t c_end = c0 + e.s;
+    const int64_t valid_end = c0 + min(e.s, max((int64_t)0, e.n - tr.r * e.s));
+    const int64_t x_beg = (c0 / kVec + tr.t * (int64_t)(kReduceThreads * kReduceVecPerThread)) * kVec;
+    const int64_t x_end = min(c_end, x_beg + (int64_t)(kReduceThreads * kReduceVecPerThread) * kVec);
+    for (int64_t x = max(x_beg, c0) + threadIdx.x; x < x_end; x += kReduceThreads) {
+        T val = T(0);
+        if (x < valid_end) {
+            const int64_t i = tr.r * e.s + (x - c0);      // padded index in the parameter
+            const int64_t r = i / s_src;
+            val = src[r * src_tab.S + o_src + (i - r * s_src)];
+        }
+        dst[x] = val;
+    }
+}
+
+// --------------------------------------------------------------------------
 // host-side validation helpers
 // --------------------------------------------------------------------------
 
@@ -925,5 +963,40 @@ extern "C" z3_status z3_scatter(const z3_layout *L, const float *full, float *sh
     if (L->psi_padded == 0) return Z3_OK;
     const ScatterArgs a{full, shards};
     for (const Tab &t : L->reduce_tabs) launch(k_scatter, t.tiles, kReduceThreads, (cudaStream_t)stream, t, a);
+    return launched(fn);
+}
+
+extern "C" z3_status z3_reshard(const z3_layout *Ls, const z3_layout *Ld, int32_t elem_bytes,
+                                const void *src, void *dst, z3_stream stream) {
+    const char *fn = "z3_reshard";
+    if (Ls == nullptr || Ld == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_reshard: layout is NULL");
+    if (elem_bytes != 2 && elem_bytes != 4)
+        return fail(Z3_ERR_INVALID_ARG, "z3_reshard: elem_bytes must be 2 or 4");
+    if (Ls->n_params != Ld->n_params || Ls->numel != Ld->numel)
+        return fail(Z3_ERR_INVALID_ARG, "z3_reshard: the layouts describe different parameters");
+    const Buf bufs[2] = {{src, elem_bytes * Ls->psi_padded, "src"},
+                         {dst, elem_bytes * Ld->psi_padded, "dst"}};
+    z3_status st = check_bufs(fn, bufs, 2);
+    if (st != Z3_OK) return st;
+    if (Ld->psi_padded == 0) return Z3_OK;
+    // parameters with elements, in the order the destination tables hold them
+    std::vector<int32_t> live;
+    for (int32_t p = 0; p < Ld->n_params; ++p)
+        if (Ld->numel[p] > 0) live.push_back(p);
+    size_t next = 0;
+    for (const Tab &t : Ld->reduce_tabs) {
+        SrcTab stab{};
+        stab.S = Ls->S;
+        for (int k = 0; k < t.count; ++k, ++next) {
+            stab.s[k] = Ls->shard_numel[live[next]];
+            stab.o[k] = Ls->shard_off[live[next]];
+        }
+        if (elem_bytes == 2)
+            launch(k_reshard<uint16_t>, t.tiles, kReduceThreads, (cudaStream_t)stream, t, stab,
+                   static_cast<const uint16_t *>(src), static_cast<uint16_t *>(dst));
+        else
+            launch(k_reshard<uint32_t>, t.tiles, kReduceThreads, (cudaStream_t)stream, t, stab,
+                   static_cast<const uint32_t *>(src), static_cast<uint32_t *>(dst));
+    }
     return launched(fn);
 }

@@ -25,7 +25,7 @@ Z3_OK, Z3_ERR_INVALID_ARG, Z3_ERR_ALIGNMENT, Z3_ERR_OVERFLOW, Z3_ERR_CUDA = rang
 EXPORTS = ("z3_layout_create", "z3_layout_destroy", "z3_layout_info", "z3_layout_params",
            "z3_stats", "z3_partition", "z3_allgather", "z3_reduce_scatter",
            "z3_adam_shard_step", "z3_reduce_scatter_adam", "z3_step_layer",
-           "z3_allreduce", "z3_scatter",
+           "z3_allreduce", "z3_scatter", "z3_reshard",
            "z3_status_string", "z3_last_error")
 
 
@@ -84,6 +84,7 @@ def load():
             "z3_step_layer": (st, [vp, vp, vp, vp, i64, f32, vp, vp, vp, hp, i64, vp]),
             "z3_allreduce": (st, [vp, vp, i64, vp, f32, vp]),
             "z3_scatter": (st, [vp, vp, vp, vp]),
+            "z3_reshard": (st, [vp, vp, i32, vp, vp, vp]),
             "z3_status_string": (ctypes.c_char_p, [st]),
             "z3_last_error": (ctypes.c_size_t, [ctypes.c_char_p, ctypes.c_size_t]),
         }
@@ -264,3 +265,15 @@ def z3_scatter(layout: Layout, full, shards, stream=None):
     _, f32 = _dtypes()
     _check(load().z3_scatter(layout.handle, _dev(full, f32, layout.psi, "full"),
                              _dev(shards, f32, layout.psi_padded, "shards"), _stream(stream)))
+
+
+def z3_reshard(src_layout: Layout, dst_layout: Layout, src, dst, stream=None):
+    """Element size from the tensors' dtype (bf16: 2 bytes, fp32: 4 bytes)."""
+    b16, f32 = _dtypes()
+    dt = b16 + f32
+    elem = 2 if src.dtype in b16 else 4
+    if (dst.dtype in b16) != (elem == 2):
+        raise ValueError("src and dst must have the same element size")
+    _check(load().z3_reshard(src_layout.handle, dst_layout.handle, elem,
+                             _dev(src, dt, src_layout.psi_padded, "src"),
+                             _dev(dst, dt, dst_layout.psi_padded, "dst"), _stream(stream)))
