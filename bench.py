@@ -355,8 +355,9 @@ def run_multi(args, world, rank, local):
         dist.init_process_group("nccl", device_id=dev)
     stream = torch.cuda.current_stream()
     sid = stream.cuda_stream
-    if args.workload == "full_step_nd16":
-        model = schedule.full_step_model(dev, seed=rank)
+    if args.workload in ("full_step_nd16", "full_step_nd16_prefetch"):
+        model = schedule.full_step_model(dev, seed=rank,
+                                         prefetch=args.workload.endswith("prefetch"))
         step_bytes, psi, launches = model.step_bytes, model.psi, model.launches_per_step()
 
         def step(i):
@@ -587,7 +588,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="layer_d1024_nd8",
                     help="layer_d1024_nd8 (default), layer_7b_nd8, layer_7b_nd64, "
-                         "full_step_nd16, or sweep_n<N>_nd<R>")
+                         "full_step_nd16[_prefetch], {dp,stage1,stage2}_d1024_nd8, "
+                         "or sweep_n<N>_nd<R>")
     ap.add_argument("--kernel-steps", type=int, default=500)
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cold-bytes", type=int, default=1536 << 20,

@@ -88,10 +88,71 @@ class Model:
                                       u.master, u.m, u.v, u.shards, hp, t, stream=stream)
 
 
-def full_step_model(dev, seed: int = 0) -> Model:
+class PrefetchModel(Model):
+    """The same step with the gather of the next unit prefetched one unit
+    ahead on a second stream ("ZeRO Stage 3: Parameter Partitioning": the
+    All-Gather for layer l+1 proceeds while layer l computes; "ZeRO Stages:
+    ...": prefetched layers occupy memory, so two transient buffers).
+
+    Backward: the gather of unit i-1 runs on the gather stream while unit i's
+    fused reduce-scatter + Adam runs on the main stream.  Ordering is by
+    events: a unit's update waits for its gather; a gather into a buffer waits
+    until the update of the unit that last used that buffer is enqueued after
+    it (the point where that unit's backward compute would have finished)."""
+
+    def __init__(self, units: list[Unit], dev):
+        super().__init__(units, dev)
+        self.bufs = [self.full, torch.empty_like(self.full)]
+        self.gstream = torch.cuda.Stream(device=dev)
+
+    def step(self, hp: dict, stream=None, t: int | None = None, on_gather=None):
+        if t is None:
+            self.t += 1
+            t = self.t
+        main = torch.cuda.current_stream() if stream is None else \
+            torch.cuda.ExternalStream(stream) if isinstance(stream, int) else stream
+        g = self.gstream
+        n = len(self.units)
+        freed = [torch.cuda.Event(), torch.cuda.Event()]
+        g.wait_stream(main)                            # shards updated by the last step
+        for i, u in enumerate(self.units):            # forward, back to back on g
+            z3.z3_allgather(u.L, u.shards, self.bufs[i % 2], stream=g.cuda_stream)
+            if on_gather is not None:
+                with torch.cuda.stream(g):
+                    on_gather("forward", i)
+        order = list(range(n - 1, -1, -1))
+        gathered = {}
+
+        def gather(i):
+            buf = self.bufs[i % 2]
+            z3.z3_allgather(self.units[i].L, self.units[i].shards, buf, stream=g.cuda_stream)
+            if on_gather is not None:
+                with torch.cuda.stream(g):
+                    on_gather("backward", i)
+            ev = torch.cuda.Event()
+            ev.record(g)
+            gathered[i] = ev
+        gather(order[0])
+        for k, i in enumerate(order):
+            u = self.units[i]
+            if k + 1 < n:
+                nxt = order[k + 1]
+                if k >= 1:
+                    g.wait_event(freed[nxt % 2])       # buffer of unit i+1 is free again
+                gather(nxt)                            # prefetch one unit ahead
+            main.wait_event(gathered[i])
+            z3.z3_reduce_scatter_adam(u.L, u.grads, u.w.grad_stride, 1.0 / u.w.n_ranks, None,
+                                      u.master, u.m, u.v, u.shards, hp, t,
+                                      stream=main.cuda_stream)
+            freed[i % 2].record(main)
+        main.wait_stream(g)
+
+
+def full_step_model(dev, seed: int = 0, prefetch: bool = False) -> Model:
     """The 24-layer d=1024 model with its [50257, 1024] embedding, N_d = 16."""
     gen = I.make_generator(seed, dev)
-    return Model([Unit(w, dev, gen) for w in I.full_step_units()], dev)
+    cls = PrefetchModel if prefetch else Model
+    return cls([Unit(w, dev, gen) for w in I.full_step_units()], dev)
 
 
 

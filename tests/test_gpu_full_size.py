@@ -227,3 +227,31 @@ def test_sweep_largest_points_sampled(z3mod, orc, n, n_ranks):
     137 GB gradient buffer; 2^31-1 at N_d = 64 would need 275 GB and is the
     capacity cap)."""
     _sweep_point(z3mod, orc, n, n_ranks, full_check=False)
+
+
+def test_full_step_with_prefetch_matches(z3mod, orc):
+    """The backward gathers prefetched one unit ahead on a second stream into
+    two transient buffers: identical results, and each backward gather still
+    sees the pre-step shards."""
+    from optimizer_state_gb300 import schedule
+    dev = torch.device("cuda")
+    plain = schedule.full_step_model(dev, seed=11)
+    pre = schedule.full_step_model(dev, seed=11, prefetch=True)
+    snaps = {}
+
+    def on_gather(phase, i):
+        if phase == "backward" and i in (0, 1, 23, 24):
+            snaps[i] = pre.bufs[i % 2][:pre.units[i].L.psi].clone()
+    before = {i: u16(pre.units[i].shards) for i in snaps or (0, 1, 23, 24)}
+    for t in (1, 2):
+        plain.step(HP)
+        pre.step(HP, on_gather=on_gather if t == 1 else None)
+        torch.cuda.synchronize()
+        if t == 1:
+            for i, buf in snaps.items():
+                O = orc.layout(pre.units[i].w.numel, 16)
+                assert np.array_equal(u16(buf), orc.allgather(O, before[i]))
+    for a, b in zip(plain.units, pre.units):
+        for k in ("master", "m", "v"):
+            assert np.array_equal(bits32(f32(getattr(a, k))), bits32(f32(getattr(b, k)))), k
+        assert np.array_equal(u16(a.shards), u16(b.shards))
