@@ -44,34 +44,55 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _bind(lib):
+    """Declare the C signatures on a loaded oracle library."""
+    vp = ctypes.c_void_p
+    i32, i64, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+    f64 = ctypes.c_double
+    lib.or_layout.argtypes = [vp, i32, i32, vp, vp, vp, _I64P, _I64P, _I64P]
+    lib.or_layout.restype = ctypes.c_int
+    lib.or_bf16_from_f32.argtypes = [f32]
+    lib.or_bf16_from_f32.restype = ctypes.c_uint16
+    lib.or_f32_from_bf16.argtypes = [ctypes.c_uint16]
+    lib.or_f32_from_bf16.restype = f32
+    lib.or_bf16_from_f32_array.argtypes = [vp, vp, i64]
+    lib.or_partition.argtypes = [vp, vp, vp, vp, i32, i32, i64, vp, vp, vp, vp, vp]
+    lib.or_allgather.argtypes = [vp, vp, vp, vp, i32, i64, vp, vp]
+    lib.or_allgather_f32.argtypes = [vp, vp, vp, vp, i32, i64, vp, vp]
+    lib.or_reduce_scatter.argtypes = [vp, vp, vp, vp, i32, i32, i64, vp, i64, vp, f32, i32]
+    lib.or_allreduce.argtypes = [i64, i32, vp, i64, vp, f32]
+    lib.or_adam_constants.argtypes = [f64, f64, f64, f64, f64, i64, vp]
+    lib.or_adam.argtypes = [i64, vp, vp, vp, vp, vp, f64, f64, f64, f64, f64, i64]
+    lib.or_step_layer.argtypes = ([vp, vp, vp, vp, i32, i32, i64, vp, vp, vp, vp, i64, f32,
+                                   vp, vp, vp, vp, vp, f64, f64, f64, f64, f64, i64])
+    lib.or_accounting.argtypes = [i64, i64, i32, _I64P, _I64P, _I64P, _I64P,
+                                  ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_double)]
+    return lib
+
+
+def build_variant(source: str, out_dir: str) -> str:
+    """Compile another copy of the oracle source (used by the mutation tests,
+    which plant mistakes in a copy to show that the pins catch them)."""
+    src = os.path.join(out_dir, "z3_oracle_variant.c")
+    with open(src, "w") as f:
+        f.write(source)
+    lib = os.path.join(out_dir, "libz3oracle_variant.so")
+    subprocess.run(["gcc", "-std=c17", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+                    "-shared", "-o", lib, src, "-lm"], check=True)
+    return lib
+
+
+def source() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            vp = ctypes.c_void_p
-            i32, i64, f32 = ctypes.c_int32, ctypes.c_int64, ctypes.c_float
-            lib.or_layout.argtypes = [vp, i32, i32, vp, vp, vp, _I64P, _I64P, _I64P]
-            lib.or_layout.restype = ctypes.c_int
-            lib.or_bf16_from_f32.argtypes = [f32]
-            lib.or_bf16_from_f32.restype = ctypes.c_uint16
-            lib.or_f32_from_bf16.argtypes = [ctypes.c_uint16]
-            lib.or_f32_from_bf16.restype = f32
-            lib.or_bf16_from_f32_array.argtypes = [vp, vp, i64]
-            lib.or_partition.argtypes = [vp, vp, vp, vp, i32, i32, i64, vp, vp, vp, vp, vp]
-            lib.or_allgather.argtypes = [vp, vp, vp, vp, i32, i64, vp, vp]
-            lib.or_allgather_f32.argtypes = [vp, vp, vp, vp, i32, i64, vp, vp]
-            lib.or_reduce_scatter.argtypes = [vp, vp, vp, vp, i32, i32, i64, vp, i64, vp, f32, i32]
-            lib.or_allreduce.argtypes = [i64, i32, vp, i64, vp, f32]
-            f64 = ctypes.c_double
-            lib.or_adam_constants.argtypes = [f64, f64, f64, f64, f64, i64, vp]
-            lib.or_adam.argtypes = [i64, vp, vp, vp, vp, vp, f64, f64, f64, f64, f64, i64]
-            lib.or_step_layer.argtypes = ([vp, vp, vp, vp, i32, i32, i64, vp, vp, vp, vp, i64, f32,
-                                           vp, vp, vp, vp, vp, f64, f64, f64, f64, f64, i64])
-            lib.or_accounting.argtypes = [i64, i64, i32, _I64P, _I64P, _I64P, _I64P,
-                                          ctypes.POINTER(ctypes.c_double),
-                                          ctypes.POINTER(ctypes.c_double)]
-            _lib = lib
+            _lib = _bind(ctypes.CDLL(build()))
     return _lib
 
 
