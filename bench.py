@@ -449,9 +449,12 @@ def run_multi(args, world, rank, local):
 
 
 def run_e2e(args, z3, L, w, rep, stream, sid, step_bytes, world):
-    """The same step through the public API with host buffers: per step the
-    gradients go host->device from pinned memory and the updated bf16 shards
-    come back device->host, inside the timed region."""
+    """The same step through the public API with host buffers.  Every step
+    uploads its gradients host->device from pinned memory and reads the
+    updated bf16 shards back device->host, inside the timed region.  The
+    upload of step i+1 (into a second gradient buffer) runs on a copy stream
+    while step i computes and its result is read back; a step's update waits
+    for the previous read-back, so no copy ever sees a half-written buffer."""
     import torch
     k = max(3, min(args.steps, args.e2e_steps))
     host_grads = torch.empty(rep.grads.shape, dtype=rep.grads.dtype, pin_memory=True)
@@ -459,28 +462,58 @@ def run_e2e(args, z3, L, w, rep, stream, sid, step_bytes, world):
     host_out = torch.empty(rep.shards.shape, dtype=rep.shards.dtype, pin_memory=True)
     h2d = host_grads.numel() * host_grads.element_size()
     d2h = host_out.numel() * host_out.element_size()
-    for _ in range(2):
-        rep.grads.copy_(host_grads, non_blocking=True)
-        rep.step += 1
-        z3.z3_step_layer(L, rep.shards, rep.full, rep.grads, w.grad_stride, 1.0 / w.n_ranks,
-                         rep.master, rep.m, rep.v, HP, rep.step, stream=sid)
-        host_out.copy_(rep.shards, non_blocking=True)
+    bufs = [rep.grads, torch.empty_like(rep.grads)]
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def run(n):
+        read = None                     # read-back of the previous step done
+        done = [None, None]             # compute finished with gradient buffer b
+
+        def upload(i):
+            b = i % 2
+            if done[b] is not None:
+                up.wait_event(done[b])  # step i-2 no longer reads this buffer
+            with torch.cuda.stream(up):
+                bufs[b].copy_(host_grads, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(up)
+            return ev
+        arrived = {0: upload(0)}
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                arrived[i + 1] = upload(i + 1)   # overlaps step i
+            stream.wait_event(arrived[i])
+            if read is not None:
+                stream.wait_event(read)          # step i-1's shards have been read back
+            rep.step += 1
+            z3.z3_step_layer(L, rep.shards, rep.full, bufs[b], w.grad_stride, 1.0 / w.n_ranks,
+                             rep.master, rep.m, rep.v, HP, rep.step, stream=sid)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            done[b] = ev
+            down.wait_event(ev)
+            with torch.cuda.stream(down):
+                host_out.copy_(rep.shards, non_blocking=True)
+            read = torch.cuda.Event()
+            read.record(down)
+        stream.wait_stream(down)
+        stream.wait_stream(up)
+    run(2)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(k):
-        rep.grads.copy_(host_grads, non_blocking=True)
-        rep.step += 1
-        z3.z3_step_layer(L, rep.shards, rep.full, rep.grads, w.grad_stride, 1.0 / w.n_ranks,
-                         rep.master, rep.m, rep.v, HP, rep.step, stream=sid)
-        host_out.copy_(rep.shards, non_blocking=True)
+    up.wait_event(e0)
+    down.wait_event(e0)
+    run(k)
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
     return {"value": round(world * step_bytes * k / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k,
-            "ms_per_step": round(ms / k, 6)}
+            "ms_per_step": round(ms / k, 6),
+            "pipeline": "upload of step i+1 overlaps compute and read-back of step i"}
 
 
 # --------------------------------------------------------------------------

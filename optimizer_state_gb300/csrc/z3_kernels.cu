@@ -30,6 +30,7 @@
 // round-to-nearest-even conversion.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cmath>
 #include <cstdint>
@@ -733,6 +734,16 @@ z3_status launched(const char *fn) {
     return Z3_OK;
 }
 
+// Host-side NVTX range around the launches of one call, named after the
+// collective it enqueues, so a trace shows the AllGather / ReduceScatter /
+// update pattern of "The ZeRO-3 Diagram Most People Remember Is Wrong", s.6.
+struct Range {
+    explicit Range(const char *name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    Range(const Range &) = delete;
+    Range &operator=(const Range &) = delete;
+};
+
 // Launches a kernel with programmatic stream serialisation allowed.
 template <typename... KArgs, typename... Args>
 void launch(void (*kernel)(KArgs...), int64_t grid, int block, cudaStream_t stream,
@@ -816,6 +827,7 @@ extern "C" z3_status z3_allgather(const z3_layout *L, const uint16_t *shards, ui
     z3_status st = check_bufs(fn, bufs, 2);
     if (st != Z3_OK) return st;
     if (L->psi == 0) return Z3_OK;
+    Range range("z3/AllGather");
     return run_allgather(L, shards, full, (cudaStream_t)stream);
 }
 
@@ -838,6 +850,7 @@ extern "C" z3_status z3_reduce_scatter(const z3_layout *L, const uint16_t *grads
     a.stride = grad_stride;
     a.scale = scale;
     a.out = grad_shards;
+    Range range(accumulate ? "z3/ReduceScatter+acc" : "z3/ReduceScatter");
     return run_reduce(L, a, accumulate ? kRSAcc : kRS, (cudaStream_t)stream, fn);
 }
 
@@ -863,6 +876,7 @@ extern "C" z3_status z3_adam_shard_step(const z3_layout *L, float *master, float
     a.total = T;
     const int64_t blocks = (T + (int64_t)kAdamThreads * kVec - 1) / ((int64_t)kAdamThreads * kVec);
     if (blocks > 0x7fffffff) return fail(Z3_ERR_OVERFLOW, "z3_adam_shard_step: grid too large");
+    Range range("z3/Adam(shard)");
     launch(k_adam, blocks, kAdamThreads, (cudaStream_t)stream, a);
     return launched(fn);
 }
@@ -912,6 +926,7 @@ extern "C" z3_status z3_reduce_scatter_adam(const z3_layout *L, const uint16_t *
                                    shards, nullptr, hp, step, &a);
     if (st != Z3_OK) return st;
     if (L->psi_padded == 0) return Z3_OK;
+    Range range("z3/ReduceScatter+Adam");
     return run_reduce(L, a, grad_acc ? kRSAccAdam : kRSAdam, (cudaStream_t)stream, fn);
 }
 
@@ -926,11 +941,19 @@ extern "C" z3_status z3_step_layer(const z3_layout *L, uint16_t *shards, uint16_
     if (st != Z3_OK) return st;
     if (L->psi_padded == 0) return Z3_OK;
     const cudaStream_t s = (cudaStream_t)stream;
+    Range range("z3/step_layer");
     // forward AllGather, backward AllGather, then ReduceScatter + Adam
-    st = run_allgather(L, shards, full, s);
+    {
+        Range r1("z3/AllGather(forward)");
+        st = run_allgather(L, shards, full, s);
+    }
     if (st != Z3_OK) return st;
-    st = run_allgather(L, shards, full, s);
+    {
+        Range r2("z3/AllGather(backward)");
+        st = run_allgather(L, shards, full, s);
+    }
     if (st != Z3_OK) return st;
+    Range r3("z3/ReduceScatter+Adam");
     return run_reduce(L, a, kRSAdam, s, fn);
 }
 
@@ -949,6 +972,7 @@ extern "C" z3_status z3_allreduce(const z3_layout *L, const uint16_t *grads, int
     const int64_t blocks = (L->psi + (int64_t)kFlatThreads * kVec - 1) / ((int64_t)kFlatThreads * kVec);
     if (blocks > 0x7fffffff) return fail(Z3_ERR_OVERFLOW, "z3_allreduce: grid too large");
     const AllreduceArgs a{grads, grad_stride, out, L->psi, scale, L->n_ranks};
+    Range range("z3/AllReduce");
     launch(k_allreduce, blocks, kFlatThreads, (cudaStream_t)stream, a);
     return launched(fn);
 }
