@@ -448,6 +448,67 @@ def run_multi(args, world, rank, local):
             "gpu_launches": launches * args.steps}), flush=True)
 
 
+def run_kernels(args, local):
+    """Every device entry point alone on one layer (kernels_<layer workload>):
+    mean CUDA-event time per call over rotating replicas, algorithmic GB/s
+    and the fraction of the measured copy peak."""
+    import torch
+    from optimizer_state_gb300 import build as libbuild
+    from optimizer_state_gb300 import inputs as I
+    from optimizer_state_gb300 import schedule, z3
+    libbuild.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    w = layer_workload(args.workload[len("kernels_"):])
+    N = w.n_ranks
+    reps = [schedule.Unit(w, dev, I.make_generator(i, dev)) for i in range(3)]
+    L = reps[0].L
+    L2 = z3.Layout(w.numel, 2 * N)
+    bufs = [dict(full=torch.empty(L.psi, dtype=torch.bfloat16, device=dev),
+                 gs=torch.zeros(L.psi_padded, dtype=torch.float32, device=dev),
+                 gf=torch.empty(L.psi, dtype=torch.float32, device=dev),
+                 rs=torch.empty(L2.psi_padded, dtype=torch.float32, device=dev))
+            for _ in reps]
+    st = L.stats()
+    psi = L.psi
+    sc = 1.0 / N
+    calls = {
+        "allgather": (st["hbm_allgather"], lambda u, b, t: z3.z3_allgather(u.L, u.shards, b["full"])),
+        "reduce_scatter": (st["hbm_reduce_scatter"], lambda u, b, t: z3.z3_reduce_scatter(
+            u.L, u.grads, w.grad_stride, b["gs"], sc)),
+        "reduce_scatter_accumulate": (st["hbm_reduce_scatter_accumulate"],
+                                      lambda u, b, t: z3.z3_reduce_scatter(
+                                          u.L, u.grads, w.grad_stride, b["gs"], sc, accumulate=True)),
+        "adam_shard_step": (st["hbm_adam"], lambda u, b, t: z3.z3_adam_shard_step(
+            u.L, u.master, u.m, u.v, b["gs"], u.shards, HP, t)),
+        "reduce_scatter_adam": (st["hbm_reduce_scatter_adam"], lambda u, b, t: z3.z3_reduce_scatter_adam(
+            u.L, u.grads, w.grad_stride, sc, None, u.master, u.m, u.v, u.shards, HP, t)),
+        "allreduce": ((2 * N + 4) * psi, lambda u, b, t: z3.z3_allreduce(
+            u.L, u.grads, w.grad_stride, b["gf"], sc)),
+        "scatter": (8 * psi, lambda u, b, t: z3.z3_scatter(u.L, b["gf"], b["gs"])),
+        "reshard_fp32_to_2N": (8 * psi, lambda u, b, t: z3.z3_reshard(u.L, L2, u.master, b["rs"])),
+    }
+    peak, kind = measured_hbm_peak()
+    out = {}
+    for name, (nbytes, fn) in calls.items():
+        for i in range(args.warmup):
+            fn(reps[i % 3], bufs[i % 3], i + 1)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(args.steps):
+            fn(reps[i % 3], bufs[i % 3], i + 1)
+        e1.record()
+        torch.cuda.synchronize()
+        us = 1e3 * e0.elapsed_time(e1) / args.steps
+        gbs = nbytes / (us * 1e-6) / 1e9
+        out[name] = {"us": round(us, 3), "gbs": round(gbs, 1),
+                     "bytes_per_param": round(nbytes / psi, 3), "frac": round(gbs / peak, 4)}
+    print(json.dumps({"workload": args.workload, "psi": psi, "n_ranks": N, "peak": peak,
+                      "peak_kind": kind, "steps": args.steps,
+                      "l2": "3 rotating replicas", "kernels": out}), flush=True)
+
+
 def run_e2e(args, z3, L, w, rep, stream, sid, step_bytes, world):
     """The same step through the public API with host buffers.  Every step
     uploads its gradients host->device from pinned memory and reads the
@@ -641,6 +702,8 @@ def main():
         run_reference(args, world, rank)
     elif args.workload in LAYER_WORKLOADS:
         run_cuda(args, world, rank, local)
+    elif args.workload.startswith("kernels_"):
+        run_kernels(args, local)
     else:
         run_multi(args, world, rank, local)
 

@@ -610,7 +610,9 @@ struct ScatterArgs {
     float *__restrict__ shards;
 };
 
-// Element-wise over each reduce tile (coalesced 4-byte accesses).
+// One vector (8 elements) per thread of each reduce tile: a 32-byte copy
+// when the whole vector is valid and the table's chunks have phase 0 (the
+// source is then 32-byte aligned too), element by element otherwise.
 __global__ void __launch_bounds__(kReduceThreads) k_scatter(const __grid_constant__ Tab tab,
                                                             const ScatterArgs a) {
     pdl_enter();
@@ -620,10 +622,19 @@ __global__ void __launch_bounds__(kReduceThreads) k_scatter(const __grid_constan
     const int64_t c_end = c0 + e.s;
     const int64_t valid_end = c0 + min(e.s, max((int64_t)0, e.n - tr.r * e.s));
     const int64_t delta = e.F + tr.r * e.s - c0;
-    const int64_t x_beg = (c0 / kVec + tr.t * (int64_t)(kReduceThreads * kReduceVecPerThread)) * kVec;
-    const int64_t x_end = min(c_end, x_beg + (int64_t)(kReduceThreads * kReduceVecPerThread) * kVec);
-    for (int64_t x = max(x_beg, c0) + threadIdx.x; x < x_end; x += kReduceThreads)
+    const int64_t x0 = (c0 / kVec + tr.t * (int64_t)kReduceThreads + threadIdx.x) * kVec;
+    if (x0 >= c_end) return;
+    if (tab.phase0 && x0 >= c0 && x0 + kVec <= valid_end) {
+        float f[8];
+        ld8f(a.full + x0 + delta, f);
+        st8f(a.shards + x0, f);
+        return;
+    }
+    for (int l = 0; l < kVec; ++l) {
+        const int64_t x = x0 + l;
+        if (x < c0 || x >= c_end) continue;
         a.shards[x] = x < valid_end ? a.full[x + delta] : 0.0f;
+    }
 }
 
 // --------------------------------------------------------------------------
@@ -638,10 +649,14 @@ struct SrcTab {
     int64_t o[kTabMax];
 };
 
+// One destination vector per thread: a run of 8 consecutive padded indices
+// of one parameter, read from one or more source ranks' slices with a
+// single division per vector, stored with 16-byte stores.
 template <typename T>
 __global__ void __launch_bounds__(kReduceThreads)
 k_reshard(const __grid_constant__ Tab tab, const __grid_constant__ SrcTab src_tab,
           const T *__restrict__ src, T *__restrict__ dst) {
+    static_assert(sizeof(T) == 2 || sizeof(T) == 4, "bf16 or fp32 words");
     pdl_enter();
     const TileRef tr = locate(tab, blockIdx.x);
     const TabEntry &e = tab.e[tr.p];
@@ -650,12 +665,40 @@ k_reshard(const __grid_constant__ Tab tab, const __grid_constant__ SrcTab src_ta
     const int64_t c0 = tr.r * tab.S + e.o;
     const int64_t c_end = c0 + e.s;
     const int64_t valid_end = c0 + min(e.s, max((int64_t)0, e.n - tr.r * e.s));
-    const int64_t x_beg = (c0 / kVec + tr.t * (int64_t)(kReduceThreads * kReduceVecPerThread)) * kVec;
-    const int64_t x_end = min(c_end, x_beg + (int64_t)(kReduceThreads * kReduceVecPerThread) * kVec);
-    for (int64_t x = max(x_beg, c0) + threadIdx.x; x < x_end; x += kReduceThreads) {
+    const int64_t x0 = (c0 / kVec + tr.t * (int64_t)kReduceThreads + threadIdx.x) * kVec;
+    if (x0 >= c_end) return;
+    if (x0 >= c0 && x0 + kVec <= valid_end) {
+        const int64_t i0 = tr.r * e.s + (x0 - c0);   // padded index of the first element
+        int64_t r = i0 / s_src;
+        int64_t j = i0 - r * s_src;
+        T v[8];
+#pragma unroll
+        for (int l = 0; l < 8; ++l) {
+            v[l] = src[r * src_tab.S + o_src + j];
+            if (++j == s_src) {
+                j = 0;
+                ++r;
+            }
+        }
+        if constexpr (sizeof(T) == 2) {
+            uint4 w;
+            w.x = (uint32_t)v[0] | ((uint32_t)v[1] << 16);
+            w.y = (uint32_t)v[2] | ((uint32_t)v[3] << 16);
+            w.z = (uint32_t)v[4] | ((uint32_t)v[5] << 16);
+            w.w = (uint32_t)v[6] | ((uint32_t)v[7] << 16);
+            *reinterpret_cast<uint4 *>(dst + x0) = w;
+        } else {
+            *reinterpret_cast<uint4 *>(dst + x0) = make_uint4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<uint4 *>(dst + x0 + 4) = make_uint4(v[4], v[5], v[6], v[7]);
+        }
+        return;
+    }
+    for (int l = 0; l < kVec; ++l) {
+        const int64_t x = x0 + l;
+        if (x < c0 || x >= c_end) continue;
         T val = T(0);
         if (x < valid_end) {
-            const int64_t i = tr.r * e.s + (x - c0);      // padded index in the parameter
+            const int64_t i = tr.r * e.s + (x - c0);
             const int64_t r = i / s_src;
             val = src[r * src_tab.S + o_src + (i - r * s_src)];
         }
