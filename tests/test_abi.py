@@ -140,3 +140,24 @@ def test_product_never_reaches_the_oracle():
     for f in os.listdir(os.path.join(ROOT, "oracle")):
         if f.endswith((".py", ".c")):
             assert not back.search(open(os.path.join(ROOT, "oracle", f)).read()), f
+
+
+def test_stage_and_reshard_entry_validation(lib):
+    """z3_allreduce, z3_scatter and z3_reshard reject bad arguments on the
+    host (fake device addresses; nothing reaches CUDA)."""
+    L = z3.Layout([35, 13, 12], 4)
+    A = 1 << 32
+    far = A + (1 << 28)
+    assert lib.z3_allreduce(L.handle, A, 59, far, 0.25, None) == z3.Z3_ERR_INVALID_ARG
+    assert lib.z3_allreduce(L.handle, A, 61, far, 0.25, None) == z3.Z3_ERR_ALIGNMENT
+    assert lib.z3_allreduce(L.handle, A, 64, A + 64, 0.25, None) == z3.Z3_ERR_INVALID_ARG
+    assert lib.z3_allreduce(None, A, 64, far, 0.25, None) == z3.Z3_ERR_INVALID_ARG
+    assert lib.z3_scatter(L.handle, A, A, None) == z3.Z3_ERR_INVALID_ARG
+    assert lib.z3_scatter(L.handle, A + 4, far, None) == z3.Z3_ERR_ALIGNMENT
+    L2 = z3.Layout([35, 13, 12], 8)
+    L3 = z3.Layout([35, 13, 11], 8)
+    assert lib.z3_reshard(L.handle, L2.handle, 3, A, far, None) == z3.Z3_ERR_INVALID_ARG
+    assert lib.z3_reshard(L.handle, L3.handle, 4, A, far, None) == z3.Z3_ERR_INVALID_ARG
+    assert "different parameters" in z3.last_error()
+    assert lib.z3_reshard(L.handle, L2.handle, 4, A, A + 16, None) == z3.Z3_ERR_INVALID_ARG
+    assert lib.z3_reshard(L.handle, None, 4, A, far, None) == z3.Z3_ERR_INVALID_ARG
