@@ -321,7 +321,7 @@ def run_cuda(args, world, rank, local):
         dist.destroy_process_group()
 
 
-LAYER_WORKLOADS = ("layer_d1024_nd8", "layer_7b_nd8", "layer_7b_nd64")
+LAYER_WORKLOADS = ("layer_d1024_nd8", "layer_7b_nd8", "layer_7b_nd64", "layer_primes_nd8")
 
 
 def layer_workload(name: str):
@@ -330,6 +330,8 @@ def layer_workload(name: str):
         return I.LAYER_D1024
     if name.startswith("layer_7b_nd"):
         return I.layer_7b(int(name[len("layer_7b_nd"):]))
+    if name.startswith("layer_primes_nd"):
+        return I.layer_primes(int(name[len("layer_primes_nd"):]))
     raise SystemExit(f"unknown layer workload {name}")
 
 

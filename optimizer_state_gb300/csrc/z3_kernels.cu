@@ -610,9 +610,10 @@ struct ScatterArgs {
     float *__restrict__ shards;
 };
 
-// One vector (8 elements) per thread of each reduce tile: a 32-byte copy
-// when the whole vector is valid and the table's chunks have phase 0 (the
-// source is then 32-byte aligned too), element by element otherwise.
+// One vector (8 elements) per thread of each reduce tile: when the whole
+// vector is valid, 32-byte stores (and 32-byte loads when the table's chunks
+// have phase 0, so the source is aligned too); element by element at chunk
+// edges and in the pad.
 __global__ void __launch_bounds__(kReduceThreads) k_scatter(const __grid_constant__ Tab tab,
                                                             const ScatterArgs a) {
     pdl_enter();
@@ -624,9 +625,14 @@ __global__ void __launch_bounds__(kReduceThreads) k_scatter(const __grid_constan
     const int64_t delta = e.F + tr.r * e.s - c0;
     const int64_t x0 = (c0 / kVec + tr.t * (int64_t)kReduceThreads + threadIdx.x) * kVec;
     if (x0 >= c_end) return;
-    if (tab.phase0 && x0 >= c0 && x0 + kVec <= valid_end) {
+    if (x0 >= c0 && x0 + kVec <= valid_end) {
         float f[8];
-        ld8f(a.full + x0 + delta, f);
+        if (tab.phase0) {
+            ld8f(a.full + x0 + delta, f);
+        } else {  // source 4-byte aligned only: word loads, the warp's lines come through L1
+#pragma unroll
+            for (int l = 0; l < 8; ++l) f[l] = a.full[x0 + delta + l];
+        }
         st8f(a.shards + x0, f);
         return;
     }

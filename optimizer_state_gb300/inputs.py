@@ -81,6 +81,14 @@ def layer_7b(n_ranks: int) -> Workload:
                     n_ranks=n_ranks, param_std=0.02, grad_std=1e-3)
 
 
+def layer_primes(n_ranks: int) -> Workload:
+    """A layer of three prime-length parameters: every chunk after the first
+    has a different phase between its full-space and shard-space indices,
+    so the reduce and gather kernels must shift 16-byte windows."""
+    return Workload(f"layer_primes_nd{n_ranks}", ((67108879,), (33554467,), (1048583,)),
+                    n_ranks=n_ranks, param_std=0.02, grad_std=1e-3)
+
+
 VOCAB = 50257
 FULL_STEP_LAYERS = 24
 

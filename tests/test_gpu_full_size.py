@@ -112,6 +112,16 @@ def test_layer_7b(z3mod, orc, n_ranks):
     _layer_step(z3mod, orc, I.layer_7b(n_ranks), seed=7)
 
 
+@pytest.mark.parametrize("n_ranks", [8, 3])
+def test_layer_primes_mixed_phases(z3mod, orc, n_ranks):
+    """Three prime-length parameters: the generic, window-shifting kernels."""
+    from optimizer_state_gb300 import z3
+    w = I.layer_primes(n_ranks)
+    L = z3.Layout(w.numel, n_ranks)
+    assert L.psi == 101711929
+    _layer_step(z3mod, orc, w, seed=8)
+
+
 def test_full_step_24_layers(z3mod, orc):
     """24 d=1024 layers + embedding, N_d = 16: forward gathers of every unit,
     then backward gather + fused reduce-scatter/Adam in reverse unit order,
