@@ -42,7 +42,7 @@ struct Tab {
 // Tile geometry of each kernel family (threads x vectors per thread).
 constexpr int kGatherThreads = 256;
 constexpr int kGatherVecPerThread = 2;
-constexpr int kReduceThreads = 256;
+constexpr int kReduceThreads = 128;
 constexpr int kReduceVecPerThread = 1;
 
 }  // namespace z3

@@ -448,7 +448,7 @@ __device__ __noinline__ void reduce_edges(const ReduceArgs a, int n_ranks, int64
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kReduceThreads, 4)
+__global__ void __launch_bounds__(kReduceThreads, 1024 / kReduceThreads)
 k_reduce_aligned(const __grid_constant__ Tab tab, const ReduceArgs a) {
     static_assert(kReduceVecPerThread == 1, "one vector per thread");
     pdl_enter();
