@@ -6,6 +6,7 @@ CUDA runtime.  ``python -m optimizer_state_gb300.build`` runs it by hand.
 """
 from __future__ import annotations
 
+import fcntl
 import os
 import shutil
 import subprocess
@@ -61,8 +62,18 @@ def _compile(src: str, kind: str, extra: list[str]) -> str:
 
 
 def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile (if stale) and return the path of the shared library."""
+    """Compile (if stale) and return the path of the shared library.  An
+    inter-process lock serialises concurrent callers (one process per GPU)."""
     os.makedirs(BUILD_DIR, exist_ok=True)
+    with open(os.path.join(BUILD_DIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return _build_locked(force, verbose_ptxas)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(force: bool, verbose_ptxas: bool) -> str:
     if not force and not _stale():
         return LIB_PATH
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []

@@ -13,6 +13,7 @@ citations are repeated in ``z3_oracle.c``.
 from __future__ import annotations
 
 import ctypes
+import fcntl
 import os
 import subprocess
 import threading
@@ -31,8 +32,18 @@ _I64P = ctypes.POINTER(ctypes.c_int64)
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc: -O2, no FMA contraction, no fast-math."""
+    """Compile the oracle with gcc: -O2, no FMA contraction, no fast-math
+    (serialised across processes by a lock file)."""
     os.makedirs(_BUILD_DIR, exist_ok=True)
+    with open(os.path.join(_BUILD_DIR, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return _build_locked(force)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(force: bool) -> str:
     if (not force and os.path.exists(_LIB_PATH)
             and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
         return _LIB_PATH
