@@ -1,0 +1,67 @@
+"""The C ABI from plain C: tests/c/abi_client.c allocates its own device
+memory with cudaMalloc, drives z3_partition and three z3_step_layer calls
+through include/z3.h, and its outputs must equal the oracle's bit for bit.
+No Python binding or torch tensor is involved on that path."""
+import os
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+
+
+@pytest.fixture(scope="module")
+def client(tmp_path_factory):
+    if not torch.cuda.is_available():
+        pytest.fail("CUDA is not available: the GPU tests need a GPU")
+    from optimizer_state_gb300 import build
+    lib = build.build()
+    cuda = os.path.dirname(os.path.dirname(shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"))
+    out = str(tmp_path_factory.mktemp("c") / "abi_client")
+    libdir = os.path.dirname(lib)
+    subprocess.run(["gcc", "-std=c11", "-O2", "-Wall", f"-I{ROOT}/include", f"-I{cuda}/include",
+                    os.path.join(ROOT, "tests", "c", "abi_client.c"), "-o", out, f"-L{libdir}",
+                    "-lz3", f"-L{cuda}/lib64", "-lcudart", f"-Wl,-rpath,{libdir}"], check=True)
+    return out
+
+
+@pytest.mark.parametrize("numel,n_ranks", [([35, 13, 12], 4), ([100003, 7, 1, 0, 4099], 3),
+                                           ([4096, 1024, 16], 8)])
+def test_c_client_matches_oracle(client, orc, tmp_path, numel, n_ranks):
+    rng = np.random.default_rng(3)
+    L = orc.layout(numel, n_ranks)
+    stride = -(-L.psi // 8) * 8
+    full = (rng.standard_normal(L.psi) * 0.02).astype(np.float32)
+    steps = 3
+    grads = []
+    for _ in range(steps):
+        g = np.zeros((n_ranks, stride), np.uint16)
+        g[:, :L.psi] = orc.bf16_from_f32(rng.standard_normal((n_ranks, L.psi)).astype(np.float32))
+        grads.append(g)
+    inp, outp = tmp_path / "in.bin", tmp_path / "out.bin"
+    with open(inp, "wb") as f:
+        f.write(full.tobytes())
+        for g in grads:
+            f.write(g.tobytes())
+    r = subprocess.run([client, str(inp), str(outp), str(n_ranks), str(steps), str(len(numel)),
+                        *map(str, numel)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    raw = open(outp, "rb").read()
+    T = L.psi_padded
+    sh = np.frombuffer(raw, np.uint16, T, 0)
+    ma, m, v = (np.frombuffer(raw, np.float32, T, 2 * T + 4 * T * i) for i in range(3))
+    gathered = np.frombuffer(raw, np.uint16, L.psi, 2 * T + 12 * T)
+    o_sh, o_ma, o_m, o_v = orc.partition(L, full)
+    for t, g in enumerate(grads, start=1):
+        _, fb, _ = orc.step_layer(L, o_sh, g.reshape(-1), stride, 1.0 / n_ranks, o_ma, o_m, o_v,
+                                  HP, t)
+    assert np.array_equal(sh, o_sh)
+    for got, want in ((ma, o_ma), (m, o_m), (v, o_v)):
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    assert np.array_equal(gathered, fb)
