@@ -290,11 +290,13 @@ __device__ __forceinline__ void reduce_vector(const ReduceArgs &a, int n_ranks, 
     // epilogue state: keeping the state out of the fold keeps the kernel
     // within 64 registers, and the other resident warps cover its latency.
     const uint16_t *gp = a.grads + (x0 + delta - PHI);
+    // a shifted window needs two 16-byte loads per rank: half the batch
+    constexpr int RB = PHI == 0 ? kRankBatch : kRankBatch / 2;
     float acc[8];
-    for (int k0 = 0; k0 < n_ranks; k0 += kRankBatch) {
-        uint4 lo[kRankBatch], hi[kRankBatch];
+    for (int k0 = 0; k0 < n_ranks; k0 += RB) {
+        uint4 lo[RB], hi[RB];
 #pragma unroll
-        for (int u = 0; u < kRankBatch; ++u) {
+        for (int u = 0; u < RB; ++u) {
             if (k0 + u < n_ranks) {
                 const uint16_t *rp = gp + (int64_t)(k0 + u) * a.stride;
                 lo[u] = ld_nc(rp);
@@ -302,7 +304,7 @@ __device__ __forceinline__ void reduce_vector(const ReduceArgs &a, int n_ranks, 
             }
         }
 #pragma unroll
-        for (int u = 0; u < kRankBatch; ++u) {
+        for (int u = 0; u < RB; ++u) {
             if (k0 + u < n_ranks) {
                 float f[8];
                 unpack8(window8<PHI>(lo[u], hi[u]), f);
@@ -349,69 +351,6 @@ __device__ __forceinline__ void reduce_vector(const ReduceArgs &a, int n_ranks, 
         b.z = pack_bf16x2(p[4], p[5]);
         b.w = pack_bf16x2(p[6], p[7]);
         *reinterpret_cast<uint4 *>(a.shards + x0) = b;
-    }
-}
-
-template <int PHI, int MODE>
-__device__ __forceinline__ void reduce_tile(const ReduceArgs &a, int n_ranks, int64_t c0,
-                                            int64_t c_end, int64_t valid_end, int64_t delta,
-                                            int64_t qbeg, int64_t qend) {
-#pragma unroll
-    for (int i = 0; i < kReduceVecPerThread; ++i) {
-        const int64_t q = qbeg + (int64_t)i * kReduceThreads + threadIdx.x;
-        if (q >= qend) continue;
-        const int64_t x0 = q * kVec;
-        if (x0 >= c0 && x0 + kVec <= valid_end) {
-            reduce_vector<PHI, MODE>(a, n_ranks, x0, delta);
-        } else {
-            for (int l = 0; l < kVec; ++l) {
-                const int64_t x = x0 + l;
-                if (x < c0 || x >= c_end) continue;  // another chunk's element
-                const bool pad = x >= valid_end;
-                float g = 0.0f;
-                if (!pad) {
-                    const uint16_t *gp = a.grads + (x + delta);
-                    float s = bf16_to_f32(gp[0]);
-                    for (int k = 1; k < n_ranks; ++k)
-                        s = __fadd_rn(s, bf16_to_f32(gp[(int64_t)k * a.stride]));
-                    g = __fmul_rn(s, a.scale);
-                }
-                finish1<MODE>(a, x, g, pad);
-            }
-        }
-    }
-}
-
-template <bool ALIGNED, int MODE>
-__global__ void __launch_bounds__(kReduceThreads)
-k_reduce(const __grid_constant__ Tab tab, const ReduceArgs a) {
-    pdl_enter();
-    const TileRef tr = locate(tab, blockIdx.x);
-    const TabEntry &e = tab.e[tr.p];
-    const int64_t c0 = tr.r * tab.S + e.o;
-    const int64_t c_end = c0 + e.s;
-    const int64_t valid_end = c0 + min(e.s, max((int64_t)0, e.n - tr.r * e.s));
-    const int64_t q_first = c0 / kVec;
-    const int64_t q_last = (c_end - 1) / kVec;
-    const int64_t qbeg = q_first + tr.t * (int64_t)(kReduceThreads * kReduceVecPerThread);
-    if (qbeg > q_last) return;
-    const int64_t qend = min(q_last + 1, qbeg + (int64_t)(kReduceThreads * kReduceVecPerThread));
-    const int64_t delta = e.F + tr.r * e.s - c0;
-    const int n_ranks = tab.n_ranks;
-    if constexpr (ALIGNED) {
-        reduce_tile<0, MODE>(a, n_ranks, c0, c_end, valid_end, delta, qbeg, qend);
-    } else {
-        const int phi = (int)(((delta % kVec) + kVec) % kVec);
-        switch (phi) {
-            case 0: reduce_tile<0, MODE>(a, n_ranks, c0, c_end, valid_end, delta, qbeg, qend); break;
-            case 1: reduce_tile<1, MODE>(a, n_ranks, c0, c_end, valid_end, delta, qbeg, qend); break;
-            case 2: reduce_tile<2, MODE>(a, n_ranks, c0, c_end, valid_end, delta, qbeg, qend); break;
-            case 3: reduce_tile<3, MODE>(a, n_ranks, c0, c_end, valid_end, delta, qbeg, qend); break;
-            case 4: reduce_tile<4, MODE>(a, n_ranks, c0, c_end, valid_end, delta, qbeg, qend); break;
-            case 5: reduce_tile<5, MODE>(a, n_ranks, c0, c_end, valid_end, delta, qbeg, qend); break;
-            case 6: reduce_tile<6, MODE>(a, n_ranks, c0, c_end, valid_end, delta, qbeg, qend); break;
-            default: reduce_tile<7, MODE>(a, n_ranks, c0, c_end, valid_end, delta, qbeg, qend); break;
-        }
     }
 }
 
@@ -464,6 +403,37 @@ k_reduce_aligned(const __grid_constant__ Tab tab, const ReduceArgs a) {
         reduce_vector<0, MODE>(a, tab.n_ranks, x0, delta);
     else
         reduce_edges<MODE>(a, tab.n_ranks, x0, delta, c0, c_end, valid_end);
+}
+
+// The same for tables whose chunks have other phases: each chunk's phase
+// (uniform per CTA) selects a window-shifting instantiation.
+template <int MODE>
+__global__ void __launch_bounds__(kReduceThreads, 1024 / kReduceThreads)
+k_reduce_shifted(const __grid_constant__ Tab tab, const ReduceArgs a) {
+    pdl_enter();
+    const TileRef tr = locate(tab, blockIdx.x);
+    const TabEntry &e = tab.e[tr.p];
+    const int64_t c0 = tr.r * tab.S + e.o;
+    const int64_t c_end = c0 + e.s;
+    const int64_t valid_end = c0 + min(e.s, max((int64_t)0, e.n - tr.r * e.s));
+    const int64_t delta = e.F + tr.r * e.s - c0;
+    const int64_t x0 = (c0 / kVec + tr.t * (int64_t)kReduceThreads + threadIdx.x) * kVec;
+    if (x0 >= c_end) return;
+    if (!(x0 >= c0 && x0 + kVec <= valid_end)) {
+        reduce_edges<MODE>(a, tab.n_ranks, x0, delta, c0, c_end, valid_end);
+        return;
+    }
+    const int n = tab.n_ranks;
+    switch ((int)(((delta % kVec) + kVec) % kVec)) {
+        case 0: reduce_vector<0, MODE>(a, n, x0, delta); break;
+        case 1: reduce_vector<1, MODE>(a, n, x0, delta); break;
+        case 2: reduce_vector<2, MODE>(a, n, x0, delta); break;
+        case 3: reduce_vector<3, MODE>(a, n, x0, delta); break;
+        case 4: reduce_vector<4, MODE>(a, n, x0, delta); break;
+        case 5: reduce_vector<5, MODE>(a, n, x0, delta); break;
+        case 6: reduce_vector<6, MODE>(a, n, x0, delta); break;
+        default: reduce_vector<7, MODE>(a, n, x0, delta); break;
+    }
 }
 
 // --------------------------------------------------------------------------
@@ -828,7 +798,7 @@ z3_status launch_reduce(const Tab &t, const ReduceArgs &a, cudaStream_t stream) 
     if (t.phase0)
         launch(k_reduce_aligned<MODE>, t.tiles, kReduceThreads, stream, t, a);
     else
-        launch(k_reduce<false, MODE>, t.tiles, kReduceThreads, stream, t, a);
+        launch(k_reduce_shifted<MODE>, t.tiles, kReduceThreads, stream, t, a);
     return Z3_OK;
 }
 
