@@ -357,14 +357,18 @@ def run_multi(args, world, rank, local):
         dist.init_process_group("nccl", device_id=dev)
     stream = torch.cuda.current_stream()
     sid = stream.cuda_stream
-    if args.workload in ("full_step_nd16", "full_step_nd16_prefetch"):
-        model = schedule.full_step_model(dev, seed=rank,
-                                         prefetch=args.workload.endswith("prefetch"))
+    if args.workload.startswith("full_step_nd16"):
+        # full_step_nd16[_prefetch][_bucket<k>]
+        bucket = 1
+        if "_bucket" in args.workload:
+            bucket = int(args.workload.split("_bucket")[1])
+        model = schedule.full_step_model(dev, seed=rank, prefetch="_prefetch" in args.workload,
+                                         bucket_layers=bucket)
         step_bytes, psi, launches = model.step_bytes, model.psi, model.launches_per_step()
 
         def step(i):
             model.step(HP, stream=sid)
-        extra = {"units": len(model.units), "n_ranks": 16,
+        extra = {"units": len(model.units), "n_ranks": 16, "bucket_layers": bucket,
                  "bytes_per_param": 66, "transient_buffer_elems": model.full.numel()}
     elif args.workload.startswith("sweep_n"):
         n_s, nd_s = args.workload[len("sweep_n"):].split("_nd")

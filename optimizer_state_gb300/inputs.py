@@ -93,13 +93,17 @@ VOCAB = 50257
 FULL_STEP_LAYERS = 24
 
 
-def full_step_units() -> list[Workload]:
+def full_step_units(bucket_layers: int = 1) -> list[Workload]:
     """24-layer d=1024 model plus the [50257, 1024] embedding, N = 16.
-    Unit 0 is the embedding, units 1..24 the layers."""
+    Unit 0 is the embedding; then buckets of `bucket_layers` consecutive
+    layers, each bucket one unit whose parameter list is its layers'
+    parameters in order (a last bucket may hold fewer layers)."""
     units = [Workload("embed", ((VOCAB, 1024),), n_ranks=16, param_std=0.02, grad_std=1e-3)]
-    for i in range(FULL_STEP_LAYERS):
-        units.append(Workload(f"layer{i}", transformer_layer_shapes(1024, 4096, gated=False),
-                              n_ranks=16, param_std=0.02, grad_std=1e-3))
+    layer = transformer_layer_shapes(1024, 4096, gated=False)
+    for i in range(0, FULL_STEP_LAYERS, bucket_layers):
+        k = min(bucket_layers, FULL_STEP_LAYERS - i)
+        units.append(Workload(f"layers{i}-{i + k - 1}", layer * k, n_ranks=16, param_std=0.02,
+                              grad_std=1e-3))
     return units
 
 

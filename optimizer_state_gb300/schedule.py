@@ -38,6 +38,17 @@ class Unit:
             if grads:
                 self.grads = I.draw_grads(w, gen, dev).to(dev)
 
+    @classmethod
+    def from_full(cls, w: I.Workload, dev, master_full: torch.Tensor, grads_full: torch.Tensor):
+        """A unit built from given values: master_full is this unit's fp32
+        parameters [Psi_u]; grads_full holds its per-rank gradients as the
+        columns of a [N][>= Psi_u] tensor."""
+        u = cls(w, dev, None, grads=False)
+        z3.z3_partition(u.L, master_full.contiguous(), u.shards, u.master, u.m, u.v)
+        u.grads = torch.zeros((w.n_ranks, w.grad_stride), dtype=torch.bfloat16, device=dev)
+        u.grads[:, :w.psi].copy_(grads_full)
+        return u
+
     @property
     def step_bytes(self) -> int:
         return self.L.stats()["hbm_step_layer"]
@@ -148,11 +159,18 @@ class PrefetchModel(Model):
         main.wait_stream(g)
 
 
-def full_step_model(dev, seed: int = 0, prefetch: bool = False) -> Model:
-    """The 24-layer d=1024 model with its [50257, 1024] embedding, N_d = 16."""
+def full_step_model(dev, seed: int = 0, prefetch: bool = False, bucket_layers: int = 1) -> Model:
+    """The 24-layer d=1024 model with its [50257, 1024] embedding, N_d = 16.
+
+    bucket_layers: the parameter-bucket knob of "The ZeRO-3 Diagram Most
+    People Remember Is Wrong", s.8 -- that many consecutive layers form one
+    unit (one gather and one fused reduce-scatter + Adam launch each; the
+    transient buffer grows to the largest unit).  Every parameter is still
+    partitioned on its own, and the update is elementwise, so the result of
+    a step does not depend on the bucket size."""
     gen = I.make_generator(seed, dev)
     cls = PrefetchModel if prefetch else Model
-    return cls([Unit(w, dev, gen) for w in I.full_step_units()], dev)
+    return cls([Unit(w, dev, gen) for w in I.full_step_units(bucket_layers)], dev)
 
 
 

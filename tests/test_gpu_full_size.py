@@ -265,3 +265,46 @@ def test_full_step_with_prefetch_matches(z3mod, orc):
         for k in ("master", "m", "v"):
             assert np.array_equal(bits32(f32(getattr(a, k))), bits32(f32(getattr(b, k)))), k
         assert np.array_equal(u16(a.shards), u16(b.shards))
+
+
+@pytest.mark.parametrize("bucket", [2, 6, 24])
+def test_bucketed_full_step_matches_per_layer(z3mod, bucket):
+    """Buckets of consecutive layers (one gather and one fused update launch
+    per bucket): the parameters and fp32 state after two steps equal those of
+    the per-layer schedule, bit for bit."""
+    from optimizer_state_gb300 import schedule
+    dev = torch.device("cuda")
+    gen = I.make_generator(21, dev)
+    per = I.full_step_units(1)
+    psi = sum(w.psi for w in per)
+    master = torch.empty(psi, dtype=torch.float32, device=dev).normal_(0, 0.02, generator=gen)
+    grads = torch.empty((16, psi), dtype=torch.float32, device=dev).normal_(0, 1e-3,
+                                                                          generator=gen)
+    grads = grads.to(torch.bfloat16)
+
+    def build(units_w):
+        units, a = [], 0
+        for w in units_w:
+            units.append(schedule.Unit.from_full(w, dev, master[a:a + w.psi],
+                                                 grads[:, a:a + w.psi]))
+            a += w.psi
+        return schedule.Model(units, dev)
+    m1, mb = build(per), build(I.full_step_units(bucket))
+    assert len(mb.units) == 1 + -(-24 // bucket)
+    for _ in range(2):
+        m1.step(HP)
+        mb.step(HP)
+    torch.cuda.synchronize()
+
+    def gathered(model, name):
+        out = []
+        for u in model.units:
+            full = torch.empty(u.L.psi, dtype=torch.float32, device=dev)
+            # an fp32 gather: reshard the [N][S] buffer to one rank (S = Psi)
+            L1 = z3mod.Layout(u.w.numel, 1)
+            z3mod.z3_reshard(u.L, L1, getattr(u, name), full)
+            out.append(full)
+        return torch.cat(out)
+    for name in ("master", "m", "v"):
+        assert torch.equal(gathered(m1, name).view(torch.int32),
+                           gathered(mb, name).view(torch.int32)), name
