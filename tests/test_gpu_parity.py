@@ -158,6 +158,7 @@ ODD = [
     ([123457, 31], 1),
     ([int(x) for x in np.random.default_rng(7).integers(0, 3000, size=97)], 5),
     ([8192, 4096, 16], 8),                  # fully aligned
+    ([5000, 123], 1000),                    # 1000 ranks: most own one element or only pad
 ]
 
 
