@@ -228,3 +228,29 @@ def test_rejects_bad_arguments_on_device(z3mod):
     assert e.value.status == z3mod.Z3_ERR_ALIGNMENT
     z3mod.z3_allgather(L, sh, full)
     torch.cuda.synchronize()
+
+
+def _fuzz_layouts(n=24, seed=123):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        P = int(rng.integers(1, 61))
+        kind = rng.integers(0, 3, size=P)
+        sizes = np.where(kind == 0, rng.integers(0, 40, size=P),
+                         np.where(kind == 1, rng.integers(0, 5000, size=P),
+                                  rng.integers(0, 60000, size=P)))
+        N = int(rng.choice([1, 2, 3, 4, 5, 6, 7, 8, 9, 16, 64, 100]))
+        out.append(([int(x) for x in sizes], N))
+    return out
+
+
+FUZZ = _fuzz_layouts()
+
+
+@pytest.mark.parametrize("numel,n_ranks", FUZZ, ids=[f"fuzz{i}" for i in range(len(FUZZ))])
+def test_all_calls_fuzzed_layouts(z3mod, orc, numel, n_ranks):
+    """Seeded random layouts (empty, tiny and large parameters, up to 60 of
+    them, rank counts up to 100): every call bit-exact against the oracle."""
+    if sum(numel) == 0:
+        numel = numel + [1]
+    run_all_calls(z3mod, orc, numel, n_ranks, seed=5, steps=1)
