@@ -254,3 +254,24 @@ def test_all_calls_fuzzed_layouts(z3mod, orc, numel, n_ranks):
     if sum(numel) == 0:
         numel = numel + [1]
     run_all_calls(z3mod, orc, numel, n_ranks, seed=5, steps=1)
+
+
+def test_wide_gradient_pitch_and_late_steps(z3mod, orc):
+    """Rank rows further apart than required (pitch 96 elements beyond Psi,
+    a multiple of 8) and step counts where the bias corrections round to 1."""
+    numel, N = [4099, 77, 1024, 13], 8
+    c = Case(z3mod, orc, numel, N, seed=17)
+    stride = c.w.grad_stride + 96
+    for step in (1, 1000, 10 ** 6):
+        g = I.draw_grads(c.w, c.gen, "cuda")
+        wide = torch.zeros((N, stride), dtype=torch.bfloat16, device="cuda")
+        wide[:, :c.L.psi].copy_(g[:, :c.L.psi])
+        wide[:, c.L.psi:].fill_(float("nan"))        # never read
+        z3mod.z3_step_layer(c.L, c.shards.t, c.gathered.t, wide, stride, 1.0 / N, c.master.t,
+                            c.m.t, c.v.t, HP, step)
+        orc.step_layer(c.O, c.o["shards"], u16(wide).reshape(-1), stride, 1.0 / N,
+                       c.o["master"], c.o["m"], c.o["v"], HP, step)
+        assert_adam_equal(c.device_state(), c.o)
+    k = orc.adam_constants(HP["lr"], HP["beta1"], HP["beta2"], HP["eps"], 0.0, 10 ** 6)
+    assert k["rb1"] == 1.0 and k["rb2"] == 1.0
+    assert c.guards_ok()
