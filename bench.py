@@ -359,16 +359,19 @@ def run_multi(args, world, rank, local):
     sid = stream.cuda_stream
     if args.workload.startswith("full_step_nd16"):
         # full_step_nd16[_prefetch][_bucket<k>]
-        bucket = 1
+        bucket, depth = 1, 0
         if "_bucket" in args.workload:
             bucket = int(args.workload.split("_bucket")[1])
-        model = schedule.full_step_model(dev, seed=rank, prefetch="_prefetch" in args.workload,
-                                         bucket_layers=bucket)
+        if "_prefetch" in args.workload:
+            digits = args.workload.split("_prefetch")[1].split("_")[0]
+            depth = int(digits) if digits else 1
+        model = schedule.full_step_model(dev, seed=rank, prefetch=depth, bucket_layers=bucket)
         step_bytes, psi, launches = model.step_bytes, model.psi, model.launches_per_step()
 
         def step(i):
             model.step(HP, stream=sid)
         extra = {"units": len(model.units), "n_ranks": 16, "bucket_layers": bucket,
+                 "prefetch_depth": depth,
                  "bytes_per_param": 66, "transient_buffer_elems": model.full.numel()}
     elif args.workload.startswith("sweep_n"):
         n_s, nd_s = args.workload[len("sweep_n"):].split("_nd")
@@ -432,12 +435,23 @@ def run_multi(args, world, rank, local):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark(True)
     e0.record(stream)
     for i in range(args.steps):
         step(args.warmup + i)
     e1.record(stream)
     torch.cuda.synchronize()
+    clocks.mark(False)
+    if world > 1:
+        dist.barrier()
+    clock_info = clocks.stop()
     ms_max = max_over_ranks(e0.elapsed_time(e1), world, dev)
     value = aggregate_gbs(world, step_bytes, args.steps, ms_max)
     if rank == 0:
@@ -451,7 +465,7 @@ def run_multi(args, world, rank, local):
             "params_per_s": round(world * psi * args.steps / (ms_max * 1e-3), 1),
             "pct_of_8tbs": round(100.0 * value / (NOMINAL_HBM_GBS * world), 2),
             "frac_of_measured_peak": round(value / world / peak, 4), "peak_kind": kind,
-            "gpu_launches": launches * args.steps}), flush=True)
+            "clocks": clock_info, "gpu_launches": launches * args.steps}), flush=True)
 
 
 def run_kernels(args, local):

@@ -195,6 +195,40 @@ z3_status z3_step_layer(const z3_layout *layout, uint16_t *shards,
                         float *m, float *v, const z3_adam_hp *hp,
                         int64_t step, z3_stream stream);
 
+/* ---- a whole model step --------------------------------------------- */
+
+/* One unit of a model (a layer, a bucket of layers, an embedding): its
+ * layout, its [N][S] state and its gradients (as for z3_step_layer). */
+typedef struct z3_unit {
+    const z3_layout *layout;
+    uint16_t *shards;
+    float *master;
+    float *m;
+    float *v;
+    const uint16_t *grads;
+    int64_t grad_stride;
+    float scale;
+} z3_unit;
+
+/* One training step of a model of n_units units, in the schedule of [ZD]
+ * s.3 and [S3] (backward in reverse layer order): the forward AllGather of
+ * every unit in order, then for each unit in reverse order its backward
+ * AllGather followed by its fused ReduceScatter + Adam.  Every gather lands
+ * in a transient buffer that must hold the largest unit (bf16 [max Psi]).
+ *   n_full = 1: everything runs on `stream`, through full[0].
+ *   n_full = D + 1 (2..8) with gather_stream != NULL: the gathers run on
+ *     gather_stream up to D units ahead of the updates ([S3]: the gather of
+ *     the next layer proceeds while the current one computes; [ZS]: the
+ *     prefetch depth trades memory -- one more buffer per unit of depth --
+ *     against latency).  Unit i uses full[i mod n_full]; events order every
+ *     buffer reuse.  The call returns with `stream` ordered after all work.
+ * Results do not depend on n_full.  Errors: as z3_step_layer for each unit,
+ * n_units < 1, n_full not in 1..8, gather_stream NULL or equal to stream
+ * when n_full >= 2, overlapping buffers. */
+z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16_t *const *full,
+                        int32_t n_full, const z3_adam_hp *hp, int64_t step,
+                        z3_stream stream, z3_stream gather_stream);
+
 /* ---- stage 1 / stage 2 / plain data-parallel variants ------------------ */
 
 /* Plain data-parallel all-reduce ([S3] communication list: the baseline's

@@ -1043,3 +1043,141 @@ extern "C" z3_status z3_reshard(const z3_layout *Ls, const z3_layout *Ld, int32_
     }
     return launched(fn);
 }
+
+namespace {
+// Events used by one prefetching model step; destroyed when the step has
+// been enqueued (the runtime releases them once their work completes).
+struct Events {
+    std::vector<cudaEvent_t> ev;
+    ~Events() {
+        for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    }
+    cudaError_t make(int n) {
+        for (int i = 0; i < n; ++i) {
+            cudaEvent_t e;
+            const cudaError_t err = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+            if (err != cudaSuccess) return err;
+            ev.push_back(e);
+        }
+        return cudaSuccess;
+    }
+};
+}  // namespace
+
+extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16_t *const *full,
+                                   int32_t n_full, const z3_adam_hp *hp, int64_t step,
+                                   z3_stream stream, z3_stream gather_stream) {
+    const char *fn = "z3_model_step";
+    if (units == nullptr || n_units < 1)
+        return fail(Z3_ERR_INVALID_ARG, "z3_model_step: no units");
+    if (full == nullptr || n_full < 1 || n_full > 8)
+        return fail(Z3_ERR_INVALID_ARG, "z3_model_step: n_full must be 1..8");
+    if (n_full >= 2 && (gather_stream == nullptr || gather_stream == stream))
+        return fail(Z3_ERR_INVALID_ARG,
+                    "z3_model_step: prefetch needs a gather stream distinct from stream");
+    std::vector<ReduceArgs> args((size_t)n_units);
+    for (int32_t i = 0; i < n_units; ++i) {
+        const z3_unit &u = units[i];
+        z3_status st = prepare_rs_adam(fn, u.layout, u.grads, u.grad_stride, u.scale, nullptr,
+                                       u.master, u.m, u.v, u.shards, full[0], hp, step, &args[i]);
+        if (st != Z3_OK) return st;
+        const int64_t T = u.layout->psi_padded;
+        int64_t gbytes = 0;
+        st = check_grads(fn, u.layout, u.grad_stride, &gbytes);
+        if (st != Z3_OK) return st;
+        for (int32_t k = 1; k < n_full; ++k) {
+            const Buf bufs[7] = {{full[k], 2 * u.layout->psi, "full[k]"},
+                                 {full[0], 2 * u.layout->psi, "full[0]"},
+                                 {u.shards, 2 * T, "shards"},
+                                 {u.master, 4 * T, "master"},
+                                 {u.m, 4 * T, "m"},
+                                 {u.v, 4 * T, "v"},
+                                 {u.grads, u.layout->psi ? gbytes : 0, "grads"}};
+            st = check_bufs(fn, bufs, 7);
+            if (st != Z3_OK) return st;
+            for (int32_t j = 1; j < k; ++j) {
+                const Buf pair[2] = {{full[k], 2 * u.layout->psi, "full[k]"},
+                                     {full[j], 2 * u.layout->psi, "full[j]"}};
+                st = check_bufs(fn, pair, 2);
+                if (st != Z3_OK) return st;
+            }
+        }
+    }
+    const cudaStream_t s = (cudaStream_t)stream;
+    Range range("z3/model_step");
+    z3_status st = Z3_OK;
+    if (n_full == 1) {
+        for (int32_t i = 0; i < n_units && st == Z3_OK; ++i) {
+            Range r("z3/AllGather(forward)");
+            if (units[i].layout->psi) st = run_allgather(units[i].layout, units[i].shards, full[0], s);
+        }
+        for (int32_t i = n_units - 1; i >= 0 && st == Z3_OK; --i) {
+            const z3_layout *L = units[i].layout;
+            if (L->psi_padded == 0) continue;
+            {
+                Range r("z3/AllGather(backward)");
+                st = run_allgather(L, units[i].shards, full[0], s);
+            }
+            if (st != Z3_OK) break;
+            Range r("z3/ReduceScatter+Adam");
+            st = run_reduce(L, args[i], kRSAdam, s, fn);
+        }
+        return st;
+    }
+    // Prefetch depth D = n_full - 1: the gathers run on gather_stream up to
+    // D units ahead of the updates, unit i in buffer i mod n_full.  A gather
+    // into a buffer waits until the update of the unit that used it last
+    // (n_full units later in backward order) has run; an update waits for its
+    // unit's gather.  Gathers are enqueued before the update they run beside,
+    // so their small grids reach the GPU first.
+    // Events: 0 = entry, 1 = gathers done, 2.. = gathered[b], then freed[b].
+    const cudaStream_t g = (cudaStream_t)gather_stream;
+    const int nb = n_full;
+    Events E;
+    cudaError_t err = E.make(2 + 2 * nb);
+    auto cuda_fail = [&](cudaError_t e) {
+        return fail(Z3_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
+    };
+    auto gathered = [&](int b) { return E.ev[2 + b]; };
+    auto freed = [&](int b) { return E.ev[2 + nb + b]; };
+    if (err != cudaSuccess) return cuda_fail(err);
+    if ((err = cudaEventRecord(E.ev[0], s)) != cudaSuccess) return cuda_fail(err);
+    if ((err = cudaStreamWaitEvent(g, E.ev[0], 0)) != cudaSuccess) return cuda_fail(err);
+    for (int32_t i = 0; i < n_units && st == Z3_OK; ++i) {
+        Range r("z3/AllGather(forward)");
+        if (units[i].layout->psi) st = run_allgather(units[i].layout, units[i].shards, full[i % nb], g);
+    }
+    std::vector<bool> buffer_used((size_t)nb, false);
+    auto gather = [&](int32_t i) -> z3_status {
+        const int b = i % nb;
+        if (buffer_used[b]) {   // the unit that last used this buffer has been updated
+            cudaError_t e = cudaStreamWaitEvent(g, freed(b), 0);
+            if (e != cudaSuccess) return cuda_fail(e);
+        }
+        Range r("z3/AllGather(backward)");
+        z3_status gs = units[i].layout->psi ? run_allgather(units[i].layout, units[i].shards, full[b], g)
+                                            : Z3_OK;
+        if (gs != Z3_OK) return gs;
+        cudaError_t e = cudaEventRecord(gathered(b), g);
+        return e == cudaSuccess ? Z3_OK : cuda_fail(e);
+    };
+    const int depth = nb - 1;
+    int32_t next = n_units - 1;   // next unit to gather (backward order)
+    for (int32_t i = n_units - 1; i >= 0 && st == Z3_OK; --i) {
+        while (st == Z3_OK && next >= 0 && next >= i - depth) st = gather(next--);
+        if (st != Z3_OK) break;
+        if ((err = cudaStreamWaitEvent(s, gathered(i % nb), 0)) != cudaSuccess) return cuda_fail(err);
+        const z3_layout *L = units[i].layout;
+        if (L->psi_padded > 0) {
+            Range r("z3/ReduceScatter+Adam");
+            st = run_reduce(L, args[i], kRSAdam, s, fn);
+            if (st != Z3_OK) break;
+        }
+        if ((err = cudaEventRecord(freed(i % nb), s)) != cudaSuccess) return cuda_fail(err);
+        buffer_used[i % nb] = true;
+    }
+    if (st != Z3_OK) return st;
+    if ((err = cudaEventRecord(E.ev[1], g)) != cudaSuccess) return cuda_fail(err);
+    if ((err = cudaStreamWaitEvent(s, E.ev[1], 0)) != cudaSuccess) return cuda_fail(err);
+    return Z3_OK;
+}

@@ -78,14 +78,23 @@ class Model:
             n += 3 * tabs
         return n
 
+    def unit_args(self):
+        return [(u.L, u.shards, u.master, u.m, u.v, u.grads, u.w.grad_stride,
+                 1.0 / u.w.n_ranks) for u in self.units]
+
     def step(self, hp: dict, stream=None, t: int | None = None, on_gather=None):
-        """One training step.  `on_gather(phase, index)` (optional) is called
-        after each gather is enqueued, with the transient buffer holding that
-        unit's parameters once the stream reaches it -- the point where the
-        forward or backward compute of the unit would run."""
+        """One training step, scheduled by the library (z3_model_step).
+        With `on_gather(phase, index)` the same schedule is issued call by
+        call from here instead, and the hook is called after each gather is
+        enqueued, with the transient buffer holding that unit's parameters
+        once the stream reaches it -- the point where the forward or backward
+        compute of the unit would run."""
         if t is None:
             self.t += 1
             t = self.t
+        if on_gather is None:
+            z3.z3_model_step(self.unit_args(), [self.full], hp, t, stream=stream)
+            return
         for i, u in enumerate(self.units):            # forward
             z3.z3_allgather(u.L, u.shards, self.full, stream=stream)
             if on_gather is not None:
@@ -97,6 +106,20 @@ class Model:
                 on_gather("backward", i)
             z3.z3_reduce_scatter_adam(u.L, u.grads, u.w.grad_stride, 1.0 / u.w.n_ranks, None,
                                       u.master, u.m, u.v, u.shards, hp, t, stream=stream)
+
+
+def _torch_stream(stream):
+    """A torch stream object for a stream argument (None: the current stream;
+    an int: a raw cudaStream_t handle).  Handle 0 is the legacy default
+    stream; torch's stream wrapper treats a zero pointer as "none given" and
+    hands out a fresh pool stream instead, which would leave the work
+    unordered with everything else on the default stream, so 0 maps to
+    torch's default stream explicitly."""
+    if stream is None:
+        return torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return torch.cuda.default_stream() if stream == 0 else torch.cuda.ExternalStream(stream)
+    return stream
 
 
 class PrefetchModel(Model):
@@ -111,17 +134,23 @@ class PrefetchModel(Model):
     until the update of the unit that last used that buffer is enqueued after
     it (the point where that unit's backward compute would have finished)."""
 
-    def __init__(self, units: list[Unit], dev):
+    def __init__(self, units: list[Unit], dev, depth: int = 1):
         super().__init__(units, dev)
-        self.bufs = [self.full, torch.empty_like(self.full)]
+        self.depth = depth
+        self.bufs = [self.full] + [torch.empty_like(self.full) for _ in range(depth)]
         self.gstream = torch.cuda.Stream(device=dev)
 
     def step(self, hp: dict, stream=None, t: int | None = None, on_gather=None):
         if t is None:
             self.t += 1
             t = self.t
-        main = torch.cuda.current_stream() if stream is None else \
-            torch.cuda.ExternalStream(stream) if isinstance(stream, int) else stream
+        if on_gather is None:
+            z3.z3_model_step(self.unit_args(), self.bufs, hp, t, stream=stream,
+                             gather_stream=self.gstream)
+            return
+        if self.depth != 1:
+            raise NotImplementedError("the call-by-call schedule prefetches one unit ahead")
+        main = _torch_stream(stream)
         g = self.gstream
         n = len(self.units)
         freed = [torch.cuda.Event(), torch.cuda.Event()]
@@ -159,7 +188,7 @@ class PrefetchModel(Model):
         main.wait_stream(g)
 
 
-def full_step_model(dev, seed: int = 0, prefetch: bool = False, bucket_layers: int = 1) -> Model:
+def full_step_model(dev, seed: int = 0, prefetch: int = 0, bucket_layers: int = 1) -> Model:
     """The 24-layer d=1024 model with its [50257, 1024] embedding, N_d = 16.
 
     bucket_layers: the parameter-bucket knob of "The ZeRO-3 Diagram Most
@@ -167,10 +196,14 @@ def full_step_model(dev, seed: int = 0, prefetch: bool = False, bucket_layers: i
     unit (one gather and one fused reduce-scatter + Adam launch each; the
     transient buffer grows to the largest unit).  Every parameter is still
     partitioned on its own, and the update is elementwise, so the result of
-    a step does not depend on the bucket size."""
+    a step does not depend on the bucket size.
+
+    prefetch: how many units ahead the backward gathers run on a second stream
+    (0: none; each unit of depth costs one more transient buffer).
+    """
     gen = I.make_generator(seed, dev)
-    cls = PrefetchModel if prefetch else Model
-    return cls([Unit(w, dev, gen) for w in I.full_step_units(bucket_layers)], dev)
+    units = [Unit(w, dev, gen) for w in I.full_step_units(bucket_layers)]
+    return PrefetchModel(units, dev, int(prefetch)) if prefetch else Model(units, dev)
 
 
 

@@ -25,7 +25,7 @@ Z3_OK, Z3_ERR_INVALID_ARG, Z3_ERR_ALIGNMENT, Z3_ERR_OVERFLOW, Z3_ERR_CUDA = rang
 EXPORTS = ("z3_layout_create", "z3_layout_destroy", "z3_layout_info", "z3_layout_params",
            "z3_stats", "z3_partition", "z3_allgather", "z3_reduce_scatter",
            "z3_adam_shard_step", "z3_reduce_scatter_adam", "z3_step_layer",
-           "z3_allreduce", "z3_scatter", "z3_reshard",
+           "z3_allreduce", "z3_scatter", "z3_reshard", "z3_model_step",
            "z3_status_string", "z3_last_error")
 
 
@@ -39,6 +39,14 @@ class AdamHP(ctypes.Structure):
     _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double),
                 ("beta2", ctypes.c_double), ("eps", ctypes.c_double),
                 ("weight_decay", ctypes.c_double)]
+
+
+class Unit(ctypes.Structure):
+    """struct z3_unit."""
+    _fields_ = [("layout", ctypes.c_void_p), ("shards", ctypes.c_void_p),
+                ("master", ctypes.c_void_p), ("m", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("grads", ctypes.c_void_p), ("grad_stride", ctypes.c_int64),
+                ("scale", ctypes.c_float)]
 
 
 class Traffic(ctypes.Structure):
@@ -85,6 +93,8 @@ def load():
             "z3_allreduce": (st, [vp, vp, i64, vp, f32, vp]),
             "z3_scatter": (st, [vp, vp, vp, vp]),
             "z3_reshard": (st, [vp, vp, i32, vp, vp, vp]),
+            "z3_model_step": (st, [ctypes.POINTER(Unit), i32, ctypes.POINTER(vp), i32, hp, i64,
+                                   vp, vp]),
             "z3_status_string": (ctypes.c_char_p, [st]),
             "z3_last_error": (ctypes.c_size_t, [ctypes.c_char_p, ctypes.c_size_t]),
         }
@@ -277,3 +287,22 @@ def z3_reshard(src_layout: Layout, dst_layout: Layout, src, dst, stream=None):
     _check(load().z3_reshard(src_layout.handle, dst_layout.handle, elem,
                              _dev(src, dt, src_layout.psi_padded, "src"),
                              _dev(dst, dt, dst_layout.psi_padded, "dst"), _stream(stream)))
+
+
+def z3_model_step(units, full, hp, step: int, stream=None, gather_stream=None):
+    """units: sequence of (layout, shards, master, m, v, grads, grad_stride,
+    scale); full: one transient buffer, or two for the prefetching schedule
+    (then gather_stream is required)."""
+    b16, f32 = _dtypes()
+    arr = (Unit * len(units))()
+    for i, (L, sh, ma, m, v, g, stride, scale) in enumerate(units):
+        T = L.psi_padded
+        arr[i] = Unit(L.handle.value, _dev(sh, b16, T, "shards"), _dev(ma, f32, T, "master"),
+                      _dev(m, f32, T, "m"), _dev(v, f32, T, "v"),
+                      _dev(g, b16, L.n_ranks * stride, "grads"), stride, scale)
+    need = max(L.psi for L, *_ in units)
+    fulls = (ctypes.c_void_p * len(full))(*[_dev(f, b16, need, "full") for f in full])
+    h = _hp(hp)
+    _check(load().z3_model_step(arr, len(units), fulls, len(full), ctypes.byref(h), step,
+                                _stream(stream),
+                                None if gather_stream is None else _stream(gather_stream)))

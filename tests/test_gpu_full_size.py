@@ -308,3 +308,60 @@ def test_bucketed_full_step_matches_per_layer(z3mod, bucket):
     for name in ("master", "m", "v"):
         assert torch.equal(gathered(m1, name).view(torch.int32),
                            gathered(mb, name).view(torch.int32)), name
+
+
+@pytest.mark.parametrize("stream", [None, 0])
+@pytest.mark.parametrize("prefetch", [False, True])
+def test_native_model_step_matches_issued_schedule(z3mod, prefetch, stream):
+    """z3_model_step (the schedule inside the library) against the same
+    schedule issued call by call: identical state after three steps, with
+    the stream given as torch's current stream or as the raw handle 0 (the
+    legacy default stream, which must not turn into a stream of its own)."""
+    from optimizer_state_gb300 import schedule
+    dev = torch.device("cuda")
+    a = schedule.full_step_model(dev, seed=31, prefetch=prefetch, bucket_layers=3)
+    b = schedule.full_step_model(dev, seed=31, prefetch=prefetch, bucket_layers=3)
+    for _ in range(3):
+        a.step(HP, stream=stream)                                   # native
+        b.step(HP, stream=stream, on_gather=lambda phase, i: None)  # issued from Python
+    torch.cuda.synchronize()
+    for ua, ub in zip(a.units, b.units):
+        for k in ("master", "m", "v"):
+            assert torch.equal(getattr(ua, k).view(torch.int32), getattr(ub, k).view(torch.int32))
+        assert torch.equal(ua.shards.view(torch.int16), ub.shards.view(torch.int16))
+
+
+def test_model_step_argument_checks(z3mod):
+    from optimizer_state_gb300 import schedule
+    dev = torch.device("cuda")
+    m = schedule.full_step_model(dev, seed=1, bucket_layers=24)
+    with pytest.raises(z3mod.Z3Error):
+        z3mod.z3_model_step(m.unit_args(), [m.full, m.full], HP, 1)        # no gather stream
+    other = torch.empty_like(m.full)
+    with pytest.raises(z3mod.Z3Error):                                      # overlapping buffers
+        z3mod.z3_model_step(m.unit_args(), [m.full, other, other], HP, 1,
+                            gather_stream=torch.cuda.Stream())
+    with pytest.raises(z3mod.Z3Error):
+        z3mod.z3_model_step(m.unit_args(), [m.full], HP, 0)                # step < 1
+    small = torch.empty(16, dtype=torch.bfloat16, device=dev)
+    with pytest.raises(ValueError):
+        z3mod.z3_model_step(m.unit_args(), [small], HP, 1)                 # too small
+
+
+@pytest.mark.parametrize("depth", [2, 3])
+def test_deeper_prefetch_matches(z3mod, depth):
+    """Gathers up to `depth` units ahead (depth + 1 transient buffers): the
+    same state as the unprefetched step."""
+    from optimizer_state_gb300 import schedule
+    dev = torch.device("cuda")
+    a = schedule.full_step_model(dev, seed=41, bucket_layers=2)
+    b = schedule.full_step_model(dev, seed=41, prefetch=depth, bucket_layers=2)
+    assert len(b.bufs) == depth + 1
+    for _ in range(2):
+        a.step(HP)
+        b.step(HP)
+    torch.cuda.synchronize()
+    for ua, ub in zip(a.units, b.units):
+        for k in ("master", "m", "v"):
+            assert torch.equal(getattr(ua, k).view(torch.int32), getattr(ub, k).view(torch.int32))
+        assert torch.equal(ua.shards.view(torch.int16), ub.shards.view(torch.int16))
