@@ -24,6 +24,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import subprocess
 import sys
 import threading
@@ -76,9 +77,12 @@ def measured_hbm_peak():
 
 
 def kernel_source_digest() -> str:
+    """Digest of the sources that decide what a kernel launch does: the
+    kernels and their launchers, their argument blocks, and the layout code
+    that builds the launch tables (not the C-ABI validation layer)."""
     import hashlib
     h = hashlib.sha256()
-    for name in ("z3_kernels.cu", "z3_internal.h"):
+    for name in ("z3_kernels.cu", "z3_launch.h", "z3_internal.h", "z3_layout.cpp"):
         with open(os.path.join(ROOT, "optimizer_state_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -358,21 +362,26 @@ def run_multi(args, world, rank, local):
     stream = torch.cuda.current_stream()
     sid = stream.cuda_stream
     if args.workload.startswith("full_step_nd16"):
-        # full_step_nd16[_prefetch][_bucket<k>]
-        bucket, depth = 1, 0
-        if "_bucket" in args.workload:
-            bucket = int(args.workload.split("_bucket")[1])
-        if "_prefetch" in args.workload:
-            digits = args.workload.split("_prefetch")[1].split("_")[0]
-            depth = int(digits) if digits else 1
-        model = schedule.full_step_model(dev, seed=rank, prefetch=depth, bucket_layers=bucket)
+        # full_step_nd16[_prefetch[<D>]][_bucket<k>][_persist<T>]
+        m = re.fullmatch(r"full_step_nd16(_prefetch(\d*))?(_bucket(\d+))?(_persist(\d+))?",
+                         args.workload)
+        if m is None:
+            raise SystemExit(f"unknown workload {args.workload}")
+        depth = (int(m.group(2)) if m.group(2) else 1) if m.group(1) else 0
+        bucket = int(m.group(4)) if m.group(3) else 1
+        persist = int(m.group(6)) if m.group(5) else 0
+        model = schedule.full_step_model(dev, seed=rank, prefetch=depth, bucket_layers=bucket,
+                                         persistence_threshold=persist)
         step_bytes, psi, launches = model.step_bytes, model.psi, model.launches_per_step()
 
         def step(i):
             model.step(HP, stream=sid)
         extra = {"units": len(model.units), "n_ranks": 16, "bucket_layers": bucket,
-                 "prefetch_depth": depth,
-                 "bytes_per_param": 66, "transient_buffer_elems": model.full.numel()}
+                 "prefetch_depth": depth, "persistence_threshold": persist,
+                 "resident_params": sum(len(u.L.numel) for u in model.units
+                                        if u.resident is not None),
+                 "bytes_per_param": round(step_bytes / psi, 4),
+                 "transient_buffer_elems": model.full.numel()}
     elif args.workload.startswith("sweep_n"):
         n_s, nd_s = args.workload[len("sweep_n"):].split("_nd")
         w = I.sweep(int(n_s), int(nd_s))
@@ -582,6 +591,7 @@ def run_e2e(args, z3, L, w, rep, stream, sid, step_bytes, world):
         stream.wait_stream(up)
     run(2)
     torch.cuda.synchronize()
+    link = host_link_h2d_gbs(host_grads, bufs[1], up)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -591,10 +601,32 @@ def run_e2e(args, z3, L, w, rep, stream, sid, step_bytes, world):
     e1.record(stream)
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    return {"value": round(world * step_bytes * k / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+    value = world * step_bytes * k / (ms * 1e-3) / 1e9
+    # no step can finish faster than its upload: step bytes / (upload bytes / link rate)
+    bound = world * step_bytes / (h2d / (link * 1e9)) / 1e9
+    return {"value": round(value, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k,
             "ms_per_step": round(ms / k, 6),
-            "pipeline": "upload of step i+1 overlaps compute and read-back of step i"}
+            "pipeline": "upload of step i+1 overlaps compute and read-back of step i",
+            "host_link_h2d_gbs": round(link, 1), "upload_bound": round(bound, 2),
+            "frac_of_upload_bound": round(value / bound, 4)}
+
+
+def host_link_h2d_gbs(host, dev_buf, stream, reps: int = 5) -> float:
+    """Pinned host -> device copy rate of one upload-sized buffer, timed
+    with CUDA events on the copy stream (best of `reps`)."""
+    import torch
+    best = 0.0
+    nbytes = host.numel() * host.element_size()
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            dev_buf.copy_(host, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        best = max(best, nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+    return best
 
 
 # --------------------------------------------------------------------------
@@ -702,7 +734,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="layer_d1024_nd8",
                     help="layer_d1024_nd8 (default), layer_7b_nd8, layer_7b_nd64, "
-                         "full_step_nd16[_prefetch], {dp,stage1,stage2}_d1024_nd8, "
+                         "full_step_nd16[_prefetch[<D>]][_bucket<k>][_persist<T>], {dp,stage1,stage2}_d1024_nd8, "
                          "or sweep_n<N>_nd<R>")
     ap.add_argument("--kernel-steps", type=int, default=500)
     ap.add_argument("--e2e-steps", type=int, default=50)

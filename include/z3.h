@@ -198,7 +198,18 @@ z3_status z3_step_layer(const z3_layout *layout, uint16_t *shards,
 /* ---- a whole model step --------------------------------------------- */
 
 /* One unit of a model (a layer, a bucket of layers, an embedding): its
- * layout, its [N][S] state and its gradients (as for z3_step_layer). */
+ * layout, its [N][S] state and its gradients (as for z3_step_layer).
+ *
+ * resident: NULL for a unit whose gathered parameters are released after
+ * each use ([ZD] s.6: parameters released after use; [S3] "ZeRO Stage 3":
+ * the gathered parameters are discarded once the layer has run), so every
+ * use gathers them again into a transient buffer.  Non-NULL (bf16 [Psi] of
+ * this unit, caller-owned) for a persistent unit, the small parameters that
+ * a persistence threshold ([ZD] s.8) keeps gathered between uses: the step
+ * does not gather it forward or backward, and gathers it into `resident`
+ * once, right after its update, so the copy always holds the current
+ * parameters.  The caller fills `resident` once after z3_partition (one
+ * z3_allgather). */
 typedef struct z3_unit {
     const z3_layout *layout;
     uint16_t *shards;
@@ -208,13 +219,16 @@ typedef struct z3_unit {
     const uint16_t *grads;
     int64_t grad_stride;
     float scale;
+    uint16_t *resident;
 } z3_unit;
 
 /* One training step of a model of n_units units, in the schedule of [ZD]
  * s.3 and [S3] (backward in reverse layer order): the forward AllGather of
  * every unit in order, then for each unit in reverse order its backward
  * AllGather followed by its fused ReduceScatter + Adam.  Every gather lands
- * in a transient buffer that must hold the largest unit (bf16 [max Psi]).
+ * in a transient buffer that must hold the largest non-resident unit (bf16
+ * [max Psi]).  A resident unit instead skips both gathers and is gathered
+ * into its own buffer after its update (see z3_unit).
  *   n_full = 1: everything runs on `stream`, through full[0].
  *   n_full = D + 1 (2..8) with gather_stream != NULL: the gathers run on
  *     gather_stream up to D units ahead of the updates ([S3]: the gather of

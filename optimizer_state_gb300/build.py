@@ -1,7 +1,7 @@
 """Builds the in-tree CUDA library ``_build/libz3.so`` for sm_103a.
 
-The host translation unit goes through g++, the kernels through nvcc; both
-compile in parallel and nvcc links the shared library against the static
+The host translation units (layout, C-ABI entry points) go through g++, the
+kernels through nvcc; all compile in parallel and nvcc links the shared library against the static
 CUDA runtime.  ``python -m optimizer_state_gb300.build`` runs it by hand.
 """
 from __future__ import annotations
@@ -25,8 +25,8 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-f
               "-Xcompiler", "-Wall", f"-I{INCLUDE}"] + ARCH
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra", f"-I{INCLUDE}"]
 
-SOURCES = [("z3_layout.cpp", "cxx"), ("z3_kernels.cu", "nvcc")]
-HEADERS = ["z3_internal.h"]
+SOURCES = [("z3_layout.cpp", "cxx"), ("z3_api.cpp", "cxx"), ("z3_kernels.cu", "nvcc")]
+HEADERS = ["z3_internal.h", "z3_launch.h"]
 
 
 def _nvcc() -> str:
@@ -52,7 +52,8 @@ def _compile(src: str, kind: str, extra: list[str]) -> str:
     if kind == "nvcc":
         cmd = [_nvcc(), *NVCC_FLAGS, *extra, "-c", path, "-o", obj]
     else:
-        cmd = ["g++", *CXX_FLAGS, "-c", path, "-o", obj]
+        cuda_inc = os.path.join(os.path.dirname(os.path.dirname(_nvcc())), "include")
+        cmd = ["g++", *CXX_FLAGS, f"-I{cuda_inc}", "-c", path, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"compile failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

@@ -1,5 +1,6 @@
-// z3_kernels.cu -- sm_103a kernels of the ZeRO-3 sharded layer step and the
-// device entry points of the C ABI (include/z3.h).
+// z3_kernels.cu -- sm_103a kernels of the ZeRO-3 sharded layer step and their
+// launchers (z3_launch.h); the C-ABI entry points that validate arguments and
+// call the launchers are in z3_api.cpp.
 //
 // The N logical ranks are shard regions of this GPU's HBM, so the
 // collectives of "The ZeRO-3 Diagram Most People Remember Is Wrong", s.3
@@ -30,14 +31,10 @@
 // round-to-nearest-even conversion.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
-#include <nvtx3/nvToolsExt.h>
 
-#include <cmath>
 #include <cstdint>
-#include <string>
-#include <vector>
 
-#include "z3_internal.h"
+#include "z3_launch.h"
 
 namespace z3 {
 namespace {
@@ -96,11 +93,6 @@ __device__ __forceinline__ uint4 window8(const uint4 &lo, const uint4 &hi) {
         return r;
     }
 }
-
-// Binary32 constants of one Adam step (each rounded once on the host).
-struct AdamK {
-    float b1, c1, b2, c2, rb1, rb2, lr, eps, lwd;
-};
 
 // Kingma & Ba, Algorithm 1, in the order fixed by include/z3.h.
 __device__ __forceinline__ void adam1(float g, float &p, float &m, float &v, const AdamK &k) {
@@ -227,26 +219,6 @@ k_allgather(const __grid_constant__ Tab tab, const GatherArgs a) {
 // --------------------------------------------------------------------------
 // ReduceScatter (+ accumulate) and the fused ReduceScatter + Adam
 // --------------------------------------------------------------------------
-
-enum Mode : int {
-    kRS = 0,         // grad_shards = fold * scale
-    kRSAcc = 1,      // grad_shards = grad_shards + fold * scale
-    kRSAdam = 2,     // Adam(fold * scale)
-    kRSAccAdam = 3,  // Adam(grad_acc + fold * scale)
-};
-
-struct ReduceArgs {
-    const uint16_t *__restrict__ grads;  // [N][stride] bf16
-    int64_t stride;
-    float scale;
-    float *out;             // grad_shards (kRS, kRSAcc)
-    const float *acc_in;    // grad_acc (kRSAccAdam)
-    float *master;
-    float *m;
-    float *v;
-    uint16_t *shards;
-    AdamK k;
-};
 
 // Ranks whose 16-byte loads are issued together before they are folded.
 constexpr int kRankBatch = 8;
@@ -440,14 +412,6 @@ k_reduce_shifted(const __grid_constant__ Tab tab, const ReduceArgs a) {
 // Partition (initialisation): shard space <- full fp32, pad 0, m = v = 0
 // --------------------------------------------------------------------------
 
-struct PartitionArgs {
-    const float *__restrict__ full;
-    uint16_t *__restrict__ shards;
-    float *__restrict__ master;
-    float *__restrict__ m;
-    float *__restrict__ v;
-};
-
 __global__ void __launch_bounds__(kReduceThreads)
 k_partition(const __grid_constant__ Tab tab, const PartitionArgs a) {
     pdl_enter();
@@ -471,18 +435,6 @@ k_partition(const __grid_constant__ Tab tab, const PartitionArgs a) {
 // --------------------------------------------------------------------------
 // Adam over the flat [N][S] shard buffers
 // --------------------------------------------------------------------------
-
-struct AdamArgs {
-    float *master;
-    float *m;
-    float *v;
-    const float *grad;
-    uint16_t *shards;
-    int64_t total;
-    AdamK k;
-};
-
-constexpr int kAdamThreads = 256;
 
 __global__ void __launch_bounds__(kAdamThreads) k_adam(const AdamArgs a) {
     pdl_enter();
@@ -521,17 +473,6 @@ __global__ void __launch_bounds__(kAdamThreads) k_adam(const AdamArgs a) {
 // Plain data-parallel all-reduce into one fp32 replica, and the scatter of a
 // replicated fp32 tensor into the [N][S] shard layout (stage-1 variant)
 // --------------------------------------------------------------------------
-
-struct AllreduceArgs {
-    const uint16_t *__restrict__ grads;
-    int64_t stride;
-    float *__restrict__ out;
-    int64_t psi;
-    float scale;
-    int n_ranks;
-};
-
-constexpr int kFlatThreads = 256;
 
 // One vector of 8 full-space elements per thread: grads rows start on
 // 16-byte boundaries (stride is a multiple of 8), so every vector is aligned.
@@ -574,11 +515,6 @@ __global__ void __launch_bounds__(kFlatThreads, 4) k_allreduce(const AllreduceAr
         }
     }
 }
-
-struct ScatterArgs {
-    const float *__restrict__ full;
-    float *__restrict__ shards;
-};
 
 // One vector (8 elements) per thread of each reduce tile: when the whole
 // vector is valid, 32-byte stores (and 32-byte loads when the table's chunks
@@ -682,87 +618,6 @@ k_reshard(const __grid_constant__ Tab tab, const __grid_constant__ SrcTab src_ta
     }
 }
 
-// --------------------------------------------------------------------------
-// host-side validation helpers
-// --------------------------------------------------------------------------
-
-struct Buf {
-    const void *ptr;
-    int64_t bytes;
-    const char *name;
-};
-
-z3_status check_bufs(const char *fn, const Buf *bufs, int n) {
-    for (int i = 0; i < n; ++i) {
-        if (bufs[i].bytes == 0) continue;
-        if (bufs[i].ptr == nullptr)
-            return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": " + bufs[i].name + " is NULL");
-        if (reinterpret_cast<uintptr_t>(bufs[i].ptr) % 16 != 0)
-            return fail(Z3_ERR_ALIGNMENT,
-                        std::string(fn) + ": " + bufs[i].name + " is not 16-byte aligned");
-    }
-    for (int i = 0; i < n; ++i) {
-        for (int j = i + 1; j < n; ++j) {
-            if (bufs[i].bytes == 0 || bufs[j].bytes == 0) continue;
-            const uintptr_t a0 = reinterpret_cast<uintptr_t>(bufs[i].ptr);
-            const uintptr_t b0 = reinterpret_cast<uintptr_t>(bufs[j].ptr);
-            if (a0 < b0 + (uintptr_t)bufs[j].bytes && b0 < a0 + (uintptr_t)bufs[i].bytes)
-                return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": " + bufs[i].name +
-                                                    " overlaps " + bufs[j].name);
-        }
-    }
-    return Z3_OK;
-}
-
-z3_status check_grads(const char *fn, const z3_layout *L, int64_t grad_stride, int64_t *bytes) {
-    if (grad_stride < L->psi)
-        return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": grad_stride < psi");
-    if (grad_stride % kVec != 0)
-        return fail(Z3_ERR_ALIGNMENT,
-                    std::string(fn) + ": grad_stride is not a multiple of 8 elements");
-    int64_t elems;
-    if (__builtin_mul_overflow(grad_stride, (int64_t)L->n_ranks, &elems) ||
-        __builtin_mul_overflow(elems, (int64_t)2, bytes))
-        return fail(Z3_ERR_OVERFLOW, std::string(fn) + ": N * grad_stride overflows");
-    return Z3_OK;
-}
-
-z3_status adam_constants(const char *fn, const z3_adam_hp *hp, int64_t step, AdamK *k) {
-    if (hp == nullptr) return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": hp is NULL");
-    if (step < 1) return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": step < 1");
-    const double vals[5] = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
-    for (double x : vals)
-        if (!std::isfinite(x))
-            return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": non-finite hyperparameter");
-    k->b1 = (float)hp->beta1;
-    k->c1 = (float)(1.0 - hp->beta1);
-    k->b2 = (float)hp->beta2;
-    k->c2 = (float)(1.0 - hp->beta2);
-    k->rb1 = (float)(1.0 / (1.0 - std::pow(hp->beta1, (double)step)));
-    k->rb2 = (float)(1.0 / (1.0 - std::pow(hp->beta2, (double)step)));
-    k->lr = (float)hp->lr;
-    k->eps = (float)hp->eps;
-    k->lwd = (float)(hp->lr * hp->weight_decay);
-    return Z3_OK;
-}
-
-z3_status launched(const char *fn) {
-    const cudaError_t err = cudaGetLastError();
-    if (err != cudaSuccess)
-        return fail(Z3_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(err));
-    return Z3_OK;
-}
-
-// Host-side NVTX range around the launches of one call, named after the
-// collective it enqueues, so a trace shows the AllGather / ReduceScatter /
-// update pattern of "The ZeRO-3 Diagram Most People Remember Is Wrong", s.6.
-struct Range {
-    explicit Range(const char *name) { nvtxRangePushA(name); }
-    ~Range() { nvtxRangePop(); }
-    Range(const Range &) = delete;
-    Range &operator=(const Range &) = delete;
-};
-
 // Launches a kernel with programmatic stream serialisation allowed.
 template <typename... KArgs, typename... Args>
 void launch(void (*kernel)(KArgs...), int64_t grid, int block, cudaStream_t stream,
@@ -777,12 +632,30 @@ void launch(void (*kernel)(KArgs...), int64_t grid, int block, cudaStream_t stre
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    (void)cudaLaunchKernelEx(&cfg, kernel, args...);  // errors: cudaGetLastError in launched()
+    (void)cudaLaunchKernelEx(&cfg, kernel, args...);  // errors: cudaGetLastError below
 }
 
-// Enqueue helpers (no validation).
-z3_status run_allgather(const z3_layout *L, const uint16_t *shards, uint16_t *full,
-                        cudaStream_t stream) {
+template <int MODE>
+void launch_reduce_tab(const Tab &t, const ReduceArgs &a, cudaStream_t stream) {
+    if (t.phase0)
+        launch(k_reduce_aligned<MODE>, t.tiles, kReduceThreads, stream, t, a);
+    else
+        launch(k_reduce_shifted<MODE>, t.tiles, kReduceThreads, stream, t, a);
+}
+
+}  // namespace
+
+// --------------------------------------------------------------------------
+// launchers: enqueue only (arguments were validated by the caller)
+// --------------------------------------------------------------------------
+
+cudaError_t launch_partition(const z3_layout *L, const PartitionArgs &a, cudaStream_t stream) {
+    for (const Tab &t : L->reduce_tabs) launch(k_partition, t.tiles, kReduceThreads, stream, t, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_allgather(const z3_layout *L, const uint16_t *shards, uint16_t *full,
+                             cudaStream_t stream) {
     const GatherArgs a{shards, full};
     for (const Tab &t : L->gather_tabs) {
         if (t.phase0)
@@ -790,394 +663,57 @@ z3_status run_allgather(const z3_layout *L, const uint16_t *shards, uint16_t *fu
         else
             launch(k_allgather<false>, t.tiles, kGatherThreads, stream, t, a);
     }
-    return launched("z3_allgather");
+    return cudaGetLastError();
 }
 
-template <int MODE>
-z3_status launch_reduce(const Tab &t, const ReduceArgs &a, cudaStream_t stream) {
-    if (t.phase0)
-        launch(k_reduce_aligned<MODE>, t.tiles, kReduceThreads, stream, t, a);
-    else
-        launch(k_reduce_shifted<MODE>, t.tiles, kReduceThreads, stream, t, a);
-    return Z3_OK;
-}
-
-z3_status run_reduce(const z3_layout *L, const ReduceArgs &a, int mode, cudaStream_t stream,
-                     const char *fn) {
+cudaError_t launch_reduce(const z3_layout *L, const ReduceArgs &a, Mode mode,
+                          cudaStream_t stream) {
     for (const Tab &t : L->reduce_tabs) {
-        z3_status st;
         switch (mode) {
-            case kRS: st = launch_reduce<kRS>(t, a, stream); break;
-            case kRSAcc: st = launch_reduce<kRSAcc>(t, a, stream); break;
-            case kRSAdam: st = launch_reduce<kRSAdam>(t, a, stream); break;
-            default: st = launch_reduce<kRSAccAdam>(t, a, stream); break;
+            case kRS: launch_reduce_tab<kRS>(t, a, stream); break;
+            case kRSAcc: launch_reduce_tab<kRSAcc>(t, a, stream); break;
+            case kRSAdam: launch_reduce_tab<kRSAdam>(t, a, stream); break;
+            default: launch_reduce_tab<kRSAccAdam>(t, a, stream); break;
         }
-        if (st != Z3_OK) return st;
     }
-    return launched(fn);
+    return cudaGetLastError();
 }
 
-}  // namespace
-}  // namespace z3
-
-using namespace z3;
-
-extern "C" z3_status z3_partition(const z3_layout *L, const float *full, uint16_t *shards,
-                                  float *master, float *m, float *v, z3_stream stream) {
-    const char *fn = "z3_partition";
-    if (L == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_partition: layout is NULL");
-    const int64_t T = L->psi_padded;
-    const Buf bufs[5] = {{full, 4 * L->psi, "full"}, {shards, 2 * T, "shards"},
-                         {master, 4 * T, "master"}, {m, 4 * T, "m"}, {v, 4 * T, "v"}};
-    z3_status st = check_bufs(fn, bufs, 5);
-    if (st != Z3_OK) return st;
-    if (T == 0) return Z3_OK;
-    const PartitionArgs a{full, shards, master, m, v};
-    for (const Tab &t : L->reduce_tabs)
-        launch(k_partition, t.tiles, kReduceThreads, (cudaStream_t)stream, t, a);
-    return launched(fn);
+cudaError_t launch_adam(const AdamArgs &a, cudaStream_t stream) {
+    launch(k_adam, flat_blocks(a.total, kAdamThreads), kAdamThreads, stream, a);
+    return cudaGetLastError();
 }
 
-extern "C" z3_status z3_allgather(const z3_layout *L, const uint16_t *shards, uint16_t *full,
-                                  z3_stream stream) {
-    const char *fn = "z3_allgather";
-    if (L == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_allgather: layout is NULL");
-    const Buf bufs[2] = {{shards, 2 * L->psi_padded, "shards"}, {full, 2 * L->psi, "full"}};
-    z3_status st = check_bufs(fn, bufs, 2);
-    if (st != Z3_OK) return st;
-    if (L->psi == 0) return Z3_OK;
-    Range range("z3/AllGather");
-    return run_allgather(L, shards, full, (cudaStream_t)stream);
+cudaError_t launch_allreduce(const AllreduceArgs &a, cudaStream_t stream) {
+    launch(k_allreduce, flat_blocks(a.psi, kFlatThreads), kFlatThreads, stream, a);
+    return cudaGetLastError();
 }
 
-extern "C" z3_status z3_reduce_scatter(const z3_layout *L, const uint16_t *grads,
-                                       int64_t grad_stride, float *grad_shards, float scale,
-                                       int32_t accumulate, z3_stream stream) {
-    const char *fn = "z3_reduce_scatter";
-    if (L == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_reduce_scatter: layout is NULL");
-    if (!std::isfinite(scale)) return fail(Z3_ERR_INVALID_ARG, "z3_reduce_scatter: scale");
-    int64_t gbytes;
-    z3_status st = check_grads(fn, L, grad_stride, &gbytes);
-    if (st != Z3_OK) return st;
-    const Buf bufs[2] = {{grads, L->psi ? gbytes : 0, "grads"},
-                         {grad_shards, 4 * L->psi_padded, "grad_shards"}};
-    st = check_bufs(fn, bufs, 2);
-    if (st != Z3_OK) return st;
-    if (L->psi_padded == 0) return Z3_OK;
-    ReduceArgs a{};
-    a.grads = grads;
-    a.stride = grad_stride;
-    a.scale = scale;
-    a.out = grad_shards;
-    Range range(accumulate ? "z3/ReduceScatter+acc" : "z3/ReduceScatter");
-    return run_reduce(L, a, accumulate ? kRSAcc : kRS, (cudaStream_t)stream, fn);
+cudaError_t launch_scatter(const z3_layout *L, const ScatterArgs &a, cudaStream_t stream) {
+    for (const Tab &t : L->reduce_tabs) launch(k_scatter, t.tiles, kReduceThreads, stream, t, a);
+    return cudaGetLastError();
 }
 
-extern "C" z3_status z3_adam_shard_step(const z3_layout *L, float *master, float *m, float *v,
-                                        const float *grad_shards, uint16_t *shards,
-                                        const z3_adam_hp *hp, int64_t step, z3_stream stream) {
-    const char *fn = "z3_adam_shard_step";
-    if (L == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_adam_shard_step: layout is NULL");
-    AdamArgs a{};
-    z3_status st = adam_constants(fn, hp, step, &a.k);
-    if (st != Z3_OK) return st;
-    const int64_t T = L->psi_padded;
-    const Buf bufs[5] = {{master, 4 * T, "master"}, {m, 4 * T, "m"}, {v, 4 * T, "v"},
-                         {grad_shards, 4 * T, "grad_shards"}, {shards, 2 * T, "shards"}};
-    st = check_bufs(fn, bufs, 5);
-    if (st != Z3_OK) return st;
-    if (T == 0) return Z3_OK;
-    a.master = master;
-    a.m = m;
-    a.v = v;
-    a.grad = grad_shards;
-    a.shards = shards;
-    a.total = T;
-    const int64_t blocks = (T + (int64_t)kAdamThreads * kVec - 1) / ((int64_t)kAdamThreads * kVec);
-    if (blocks > 0x7fffffff) return fail(Z3_ERR_OVERFLOW, "z3_adam_shard_step: grid too large");
-    Range range("z3/Adam(shard)");
-    launch(k_adam, blocks, kAdamThreads, (cudaStream_t)stream, a);
-    return launched(fn);
-}
-
-namespace {
-z3_status prepare_rs_adam(const char *fn, const z3_layout *L, const uint16_t *grads,
-                          int64_t grad_stride, float scale, const float *grad_acc, float *master,
-                          float *m, float *v, uint16_t *shards, const uint16_t *extra_full,
-                          const z3_adam_hp *hp, int64_t step, ReduceArgs *a) {
-    if (L == nullptr) return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": layout is NULL");
-    if (!std::isfinite(scale)) return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": scale");
-    z3_status st = adam_constants(fn, hp, step, &a->k);
-    if (st != Z3_OK) return st;
-    int64_t gbytes;
-    st = check_grads(fn, L, grad_stride, &gbytes);
-    if (st != Z3_OK) return st;
-    const int64_t T = L->psi_padded;
-    const Buf bufs[7] = {{grads, L->psi ? gbytes : 0, "grads"},
-                         {master, 4 * T, "master"},
-                         {m, 4 * T, "m"},
-                         {v, 4 * T, "v"},
-                         {shards, 2 * T, "shards"},
-                         {grad_acc, grad_acc ? 4 * T : 0, "grad_acc"},
-                         {extra_full, extra_full ? 2 * L->psi : 0, "full"}};
-    st = check_bufs(fn, bufs, 7);
-    if (st != Z3_OK) return st;
-    a->grads = grads;
-    a->stride = grad_stride;
-    a->scale = scale;
-    a->acc_in = grad_acc;
-    a->master = master;
-    a->m = m;
-    a->v = v;
-    a->shards = shards;
-    return Z3_OK;
-}
-}  // namespace
-
-extern "C" z3_status z3_reduce_scatter_adam(const z3_layout *L, const uint16_t *grads,
-                                            int64_t grad_stride, float scale,
-                                            const float *grad_acc, float *master, float *m,
-                                            float *v, uint16_t *shards, const z3_adam_hp *hp,
-                                            int64_t step, z3_stream stream) {
-    const char *fn = "z3_reduce_scatter_adam";
-    ReduceArgs a{};
-    z3_status st = prepare_rs_adam(fn, L, grads, grad_stride, scale, grad_acc, master, m, v,
-                                   shards, nullptr, hp, step, &a);
-    if (st != Z3_OK) return st;
-    if (L->psi_padded == 0) return Z3_OK;
-    Range range("z3/ReduceScatter+Adam");
-    return run_reduce(L, a, grad_acc ? kRSAccAdam : kRSAdam, (cudaStream_t)stream, fn);
-}
-
-extern "C" z3_status z3_step_layer(const z3_layout *L, uint16_t *shards, uint16_t *full,
-                                   const uint16_t *grads, int64_t grad_stride, float scale,
-                                   float *master, float *m, float *v, const z3_adam_hp *hp,
-                                   int64_t step, z3_stream stream) {
-    const char *fn = "z3_step_layer";
-    ReduceArgs a{};
-    z3_status st = prepare_rs_adam(fn, L, grads, grad_stride, scale, nullptr, master, m, v,
-                                   shards, full, hp, step, &a);
-    if (st != Z3_OK) return st;
-    if (L->psi_padded == 0) return Z3_OK;
-    const cudaStream_t s = (cudaStream_t)stream;
-    Range range("z3/step_layer");
-    // forward AllGather, backward AllGather, then ReduceScatter + Adam
-    {
-        Range r1("z3/AllGather(forward)");
-        st = run_allgather(L, shards, full, s);
-    }
-    if (st != Z3_OK) return st;
-    {
-        Range r2("z3/AllGather(backward)");
-        st = run_allgather(L, shards, full, s);
-    }
-    if (st != Z3_OK) return st;
-    Range r3("z3/ReduceScatter+Adam");
-    return run_reduce(L, a, kRSAdam, s, fn);
-}
-
-extern "C" z3_status z3_allreduce(const z3_layout *L, const uint16_t *grads, int64_t grad_stride,
-                                  float *out, float scale, z3_stream stream) {
-    const char *fn = "z3_allreduce";
-    if (L == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_allreduce: layout is NULL");
-    if (!std::isfinite(scale)) return fail(Z3_ERR_INVALID_ARG, "z3_allreduce: scale");
-    int64_t gbytes;
-    z3_status st = check_grads(fn, L, grad_stride, &gbytes);
-    if (st != Z3_OK) return st;
-    const Buf bufs[2] = {{grads, L->psi ? gbytes : 0, "grads"}, {out, 4 * L->psi, "out"}};
-    st = check_bufs(fn, bufs, 2);
-    if (st != Z3_OK) return st;
-    if (L->psi == 0) return Z3_OK;
-    const int64_t blocks = (L->psi + (int64_t)kFlatThreads * kVec - 1) / ((int64_t)kFlatThreads * kVec);
-    if (blocks > 0x7fffffff) return fail(Z3_ERR_OVERFLOW, "z3_allreduce: grid too large");
-    const AllreduceArgs a{grads, grad_stride, out, L->psi, scale, L->n_ranks};
-    Range range("z3/AllReduce");
-    launch(k_allreduce, blocks, kFlatThreads, (cudaStream_t)stream, a);
-    return launched(fn);
-}
-
-extern "C" z3_status z3_scatter(const z3_layout *L, const float *full, float *shards,
-                                z3_stream stream) {
-    const char *fn = "z3_scatter";
-    if (L == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_scatter: layout is NULL");
-    const Buf bufs[2] = {{full, 4 * L->psi, "full"}, {shards, 4 * L->psi_padded, "shards"}};
-    z3_status st = check_bufs(fn, bufs, 2);
-    if (st != Z3_OK) return st;
-    if (L->psi_padded == 0) return Z3_OK;
-    const ScatterArgs a{full, shards};
-    for (const Tab &t : L->reduce_tabs) launch(k_scatter, t.tiles, kReduceThreads, (cudaStream_t)stream, t, a);
-    return launched(fn);
-}
-
-extern "C" z3_status z3_reshard(const z3_layout *Ls, const z3_layout *Ld, int32_t elem_bytes,
-                                const void *src, void *dst, z3_stream stream) {
-    const char *fn = "z3_reshard";
-    if (Ls == nullptr || Ld == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_reshard: layout is NULL");
-    if (elem_bytes != 2 && elem_bytes != 4)
-        return fail(Z3_ERR_INVALID_ARG, "z3_reshard: elem_bytes must be 2 or 4");
-    if (Ls->n_params != Ld->n_params || Ls->numel != Ld->numel)
-        return fail(Z3_ERR_INVALID_ARG, "z3_reshard: the layouts describe different parameters");
-    const Buf bufs[2] = {{src, elem_bytes * Ls->psi_padded, "src"},
-                         {dst, elem_bytes * Ld->psi_padded, "dst"}};
-    z3_status st = check_bufs(fn, bufs, 2);
-    if (st != Z3_OK) return st;
-    if (Ld->psi_padded == 0) return Z3_OK;
-    // parameters with elements, in the order the destination tables hold them
-    std::vector<int32_t> live;
-    for (int32_t p = 0; p < Ld->n_params; ++p)
-        if (Ld->numel[p] > 0) live.push_back(p);
-    size_t next = 0;
+cudaError_t launch_reshard(const z3_layout *Ls, const z3_layout *Ld, int elem_bytes,
+                           const void *src, void *dst, cudaStream_t stream) {
+    // the tables hold the parameters with elements, in parameter order
+    int32_t p = 0;
     for (const Tab &t : Ld->reduce_tabs) {
         SrcTab stab{};
         stab.S = Ls->S;
-        for (int k = 0; k < t.count; ++k, ++next) {
-            stab.s[k] = Ls->shard_numel[live[next]];
-            stab.o[k] = Ls->shard_off[live[next]];
+        for (int k = 0; k < t.count; ++k, ++p) {
+            while (Ld->numel[p] == 0) ++p;
+            stab.s[k] = Ls->shard_numel[p];
+            stab.o[k] = Ls->shard_off[p];
         }
         if (elem_bytes == 2)
-            launch(k_reshard<uint16_t>, t.tiles, kReduceThreads, (cudaStream_t)stream, t, stab,
+            launch(k_reshard<uint16_t>, t.tiles, kReduceThreads, stream, t, stab,
                    static_cast<const uint16_t *>(src), static_cast<uint16_t *>(dst));
         else
-            launch(k_reshard<uint32_t>, t.tiles, kReduceThreads, (cudaStream_t)stream, t, stab,
+            launch(k_reshard<uint32_t>, t.tiles, kReduceThreads, stream, t, stab,
                    static_cast<const uint32_t *>(src), static_cast<uint32_t *>(dst));
     }
-    return launched(fn);
+    return cudaGetLastError();
 }
 
-namespace {
-// Events used by one prefetching model step; destroyed when the step has
-// been enqueued (the runtime releases them once their work completes).
-struct Events {
-    std::vector<cudaEvent_t> ev;
-    ~Events() {
-        for (cudaEvent_t e : ev) cudaEventDestroy(e);
-    }
-    cudaError_t make(int n) {
-        for (int i = 0; i < n; ++i) {
-            cudaEvent_t e;
-            const cudaError_t err = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
-            if (err != cudaSuccess) return err;
-            ev.push_back(e);
-        }
-        return cudaSuccess;
-    }
-};
-}  // namespace
-
-extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16_t *const *full,
-                                   int32_t n_full, const z3_adam_hp *hp, int64_t step,
-                                   z3_stream stream, z3_stream gather_stream) {
-    const char *fn = "z3_model_step";
-    if (units == nullptr || n_units < 1)
-        return fail(Z3_ERR_INVALID_ARG, "z3_model_step: no units");
-    if (full == nullptr || n_full < 1 || n_full > 8)
-        return fail(Z3_ERR_INVALID_ARG, "z3_model_step: n_full must be 1..8");
-    if (n_full >= 2 && (gather_stream == nullptr || gather_stream == stream))
-        return fail(Z3_ERR_INVALID_ARG,
-                    "z3_model_step: prefetch needs a gather stream distinct from stream");
-    std::vector<ReduceArgs> args((size_t)n_units);
-    for (int32_t i = 0; i < n_units; ++i) {
-        const z3_unit &u = units[i];
-        z3_status st = prepare_rs_adam(fn, u.layout, u.grads, u.grad_stride, u.scale, nullptr,
-                                       u.master, u.m, u.v, u.shards, full[0], hp, step, &args[i]);
-        if (st != Z3_OK) return st;
-        const int64_t T = u.layout->psi_padded;
-        int64_t gbytes = 0;
-        st = check_grads(fn, u.layout, u.grad_stride, &gbytes);
-        if (st != Z3_OK) return st;
-        for (int32_t k = 1; k < n_full; ++k) {
-            const Buf bufs[7] = {{full[k], 2 * u.layout->psi, "full[k]"},
-                                 {full[0], 2 * u.layout->psi, "full[0]"},
-                                 {u.shards, 2 * T, "shards"},
-                                 {u.master, 4 * T, "master"},
-                                 {u.m, 4 * T, "m"},
-                                 {u.v, 4 * T, "v"},
-                                 {u.grads, u.layout->psi ? gbytes : 0, "grads"}};
-            st = check_bufs(fn, bufs, 7);
-            if (st != Z3_OK) return st;
-            for (int32_t j = 1; j < k; ++j) {
-                const Buf pair[2] = {{full[k], 2 * u.layout->psi, "full[k]"},
-                                     {full[j], 2 * u.layout->psi, "full[j]"}};
-                st = check_bufs(fn, pair, 2);
-                if (st != Z3_OK) return st;
-            }
-        }
-    }
-    const cudaStream_t s = (cudaStream_t)stream;
-    Range range("z3/model_step");
-    z3_status st = Z3_OK;
-    if (n_full == 1) {
-        for (int32_t i = 0; i < n_units && st == Z3_OK; ++i) {
-            Range r("z3/AllGather(forward)");
-            if (units[i].layout->psi) st = run_allgather(units[i].layout, units[i].shards, full[0], s);
-        }
-        for (int32_t i = n_units - 1; i >= 0 && st == Z3_OK; --i) {
-            const z3_layout *L = units[i].layout;
-            if (L->psi_padded == 0) continue;
-            {
-                Range r("z3/AllGather(backward)");
-                st = run_allgather(L, units[i].shards, full[0], s);
-            }
-            if (st != Z3_OK) break;
-            Range r("z3/ReduceScatter+Adam");
-            st = run_reduce(L, args[i], kRSAdam, s, fn);
-        }
-        return st;
-    }
-    // Prefetch depth D = n_full - 1: the gathers run on gather_stream up to
-    // D units ahead of the updates, unit i in buffer i mod n_full.  A gather
-    // into a buffer waits until the update of the unit that used it last
-    // (n_full units later in backward order) has run; an update waits for its
-    // unit's gather.  Gathers are enqueued before the update they run beside,
-    // so their small grids reach the GPU first.
-    // Events: 0 = entry, 1 = gathers done, 2.. = gathered[b], then freed[b].
-    const cudaStream_t g = (cudaStream_t)gather_stream;
-    const int nb = n_full;
-    Events E;
-    cudaError_t err = E.make(2 + 2 * nb);
-    auto cuda_fail = [&](cudaError_t e) {
-        return fail(Z3_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
-    };
-    auto gathered = [&](int b) { return E.ev[2 + b]; };
-    auto freed = [&](int b) { return E.ev[2 + nb + b]; };
-    if (err != cudaSuccess) return cuda_fail(err);
-    if ((err = cudaEventRecord(E.ev[0], s)) != cudaSuccess) return cuda_fail(err);
-    if ((err = cudaStreamWaitEvent(g, E.ev[0], 0)) != cudaSuccess) return cuda_fail(err);
-    for (int32_t i = 0; i < n_units && st == Z3_OK; ++i) {
-        Range r("z3/AllGather(forward)");
-        if (units[i].layout->psi) st = run_allgather(units[i].layout, units[i].shards, full[i % nb], g);
-    }
-    std::vector<bool> buffer_used((size_t)nb, false);
-    auto gather = [&](int32_t i) -> z3_status {
-        const int b = i % nb;
-        if (buffer_used[b]) {   // the unit that last used this buffer has been updated
-            cudaError_t e = cudaStreamWaitEvent(g, freed(b), 0);
-            if (e != cudaSuccess) return cuda_fail(e);
-        }
-        Range r("z3/AllGather(backward)");
-        z3_status gs = units[i].layout->psi ? run_allgather(units[i].layout, units[i].shards, full[b], g)
-                                            : Z3_OK;
-        if (gs != Z3_OK) return gs;
-        cudaError_t e = cudaEventRecord(gathered(b), g);
-        return e == cudaSuccess ? Z3_OK : cuda_fail(e);
-    };
-    const int depth = nb - 1;
-    int32_t next = n_units - 1;   // next unit to gather (backward order)
-    for (int32_t i = n_units - 1; i >= 0 && st == Z3_OK; --i) {
-        while (st == Z3_OK && next >= 0 && next >= i - depth) st = gather(next--);
-        if (st != Z3_OK) break;
-        if ((err = cudaStreamWaitEvent(s, gathered(i % nb), 0)) != cudaSuccess) return cuda_fail(err);
-        const z3_layout *L = units[i].layout;
-        if (L->psi_padded > 0) {
-            Range r("z3/ReduceScatter+Adam");
-            st = run_reduce(L, args[i], kRSAdam, s, fn);
-            if (st != Z3_OK) break;
-        }
-        if ((err = cudaEventRecord(freed(i % nb), s)) != cudaSuccess) return cuda_fail(err);
-        buffer_used[i % nb] = true;
-    }
-    if (st != Z3_OK) return st;
-    if ((err = cudaEventRecord(E.ev[1], g)) != cudaSuccess) return cuda_fail(err);
-    if ((err = cudaStreamWaitEvent(s, E.ev[1], 0)) != cudaSuccess) return cuda_fail(err);
-    return Z3_OK;
-}
+}  // namespace z3

@@ -42,6 +42,7 @@ class Workload:
                                                   weight_decay=0.0))
     steps: int = 1
     micro_batches: int = 1
+    resident: bool = False  # gathered once per step and kept (persistence threshold)
 
     @property
     def numel(self) -> list[int]:
@@ -93,18 +94,57 @@ VOCAB = 50257
 FULL_STEP_LAYERS = 24
 
 
-def full_step_units(bucket_layers: int = 1) -> list[Workload]:
-    """24-layer d=1024 model plus the [50257, 1024] embedding, N = 16.
-    Unit 0 is the embedding; then buckets of `bucket_layers` consecutive
-    layers, each bucket one unit whose parameter list is its layers'
-    parameters in order (a last bucket may hold fewer layers)."""
-    units = [Workload("embed", ((VOCAB, 1024),), n_ranks=16, param_std=0.02, grad_std=1e-3)]
+def _full_step_shapes() -> list[tuple]:
+    """Every parameter shape of the full-step model in model order: the
+    embedding, then the 24 layers' parameters layer by layer."""
     layer = transformer_layer_shapes(1024, 4096, gated=False)
-    for i in range(0, FULL_STEP_LAYERS, bucket_layers):
-        k = min(bucket_layers, FULL_STEP_LAYERS - i)
-        units.append(Workload(f"layers{i}-{i + k - 1}", layer * k, n_ranks=16, param_std=0.02,
-                              grad_std=1e-3))
+    return [(VOCAB, 1024)] + [sh for _ in range(FULL_STEP_LAYERS) for sh in layer]
+
+
+def full_step_param_ids(bucket_layers: int = 1, persistence_threshold: int = 0) -> list[tuple]:
+    """For each unit of full_step_units(...), the model-order indices of its
+    parameters (index 0 is the embedding, then each layer's parameters).
+
+    Unit 0 is the embedding; then buckets of `bucket_layers` consecutive
+    layers.  With persistence_threshold > 0 every parameter of fewer than
+    that many elements leaves its bucket and joins one resident unit placed
+    first: its gathered copy is kept for the whole run (updated once per
+    step), and since its gradients are complete only when the backward pass
+    has finished, it is updated last (the step runs units in reverse)."""
+    shapes = _full_step_shapes()
+    per_layer = len(transformer_layer_shapes(1024, 4096, gated=False))
+    small = {i for i, sh in enumerate(shapes) if math.prod(sh) < persistence_threshold}
+    units = [tuple(i for i in (0,) if i not in small)]
+    for l0 in range(0, FULL_STEP_LAYERS, bucket_layers):
+        k = min(bucket_layers, FULL_STEP_LAYERS - l0)
+        ids = range(1 + l0 * per_layer, 1 + (l0 + k) * per_layer)
+        units.append(tuple(i for i in ids if i not in small))
+    units = [u for u in units if u]
+    if small:
+        units.insert(0, tuple(sorted(small)))
     return units
+
+
+def full_step_units(bucket_layers: int = 1, persistence_threshold: int = 0) -> list[Workload]:
+    """24-layer d=1024 model plus the [50257, 1024] embedding, N = 16, as
+    units (see full_step_param_ids for which parameters form each unit)."""
+    shapes = _full_step_shapes()
+    ids = full_step_param_ids(bucket_layers, persistence_threshold)
+    resident = persistence_threshold > 0 and \
+        all(math.prod(shapes[i]) < persistence_threshold for i in ids[0])
+    per_layer = len(transformer_layer_shapes(1024, 4096, gated=False))
+    out = []
+    for n, u in enumerate(ids):
+        is_res = resident and n == 0
+        if is_res:
+            name = "persistent"
+        elif u == (0,):
+            name = "embed"
+        else:
+            name = f"layers{(u[0] - 1) // per_layer}-{(u[-1] - 1) // per_layer}"
+        out.append(Workload(name, tuple(shapes[i] for i in u), n_ranks=16, param_std=0.02,
+                            grad_std=1e-3, resident=is_res))
+    return out
 
 
 def next_prime(n: int) -> int:

@@ -31,12 +31,20 @@ class Unit:
         self.m = torch.empty(T, dtype=torch.float32, device=dev)
         self.v = torch.empty(T, dtype=torch.float32, device=dev)
         self.grads = None
+        # a resident unit keeps its gathered parameters for the whole run
+        self.resident = torch.empty(self.L.psi, dtype=torch.bfloat16, device=dev) \
+            if w.resident else None
         if gen is not None:
             full = I.draw_master(w, gen, dev).to(dev)
-            z3.z3_partition(self.L, full, self.shards, self.master, self.m, self.v)
+            self._partition(full)
             del full
             if grads:
                 self.grads = I.draw_grads(w, gen, dev).to(dev)
+
+    def _partition(self, full: torch.Tensor):
+        z3.z3_partition(self.L, full, self.shards, self.master, self.m, self.v)
+        if self.resident is not None:
+            z3.z3_allgather(self.L, self.shards, self.resident)
 
     @classmethod
     def from_full(cls, w: I.Workload, dev, master_full: torch.Tensor, grads_full: torch.Tensor):
@@ -44,14 +52,16 @@ class Unit:
         parameters [Psi_u]; grads_full holds its per-rank gradients as the
         columns of a [N][>= Psi_u] tensor."""
         u = cls(w, dev, None, grads=False)
-        z3.z3_partition(u.L, master_full.contiguous(), u.shards, u.master, u.m, u.v)
+        u._partition(master_full.contiguous())
         u.grads = torch.zeros((w.n_ranks, w.grad_stride), dtype=torch.bfloat16, device=dev)
         u.grads[:, :w.psi].copy_(grads_full)
         return u
 
     @property
     def step_bytes(self) -> int:
-        return self.L.stats()["hbm_step_layer"]
+        st = self.L.stats()
+        # a resident unit is gathered once per step instead of twice
+        return st["hbm_step_layer"] - (st["hbm_allgather"] if self.resident is not None else 0)
 
 
 class Model:
@@ -60,7 +70,8 @@ class Model:
     def __init__(self, units: list[Unit], dev):
         self.units = units
         self.dev = dev
-        self.full = torch.empty(max(u.L.psi for u in units), dtype=torch.bfloat16, device=dev)
+        self.full = torch.empty(max([u.L.psi for u in units if u.resident is None] or [1]),
+                                dtype=torch.bfloat16, device=dev)
         self.t = 0
 
     @property
@@ -75,12 +86,19 @@ class Model:
         n = 0
         for u in self.units:
             tabs = -(-sum(1 for x in u.L.numel if x > 0) // 40)
-            n += 3 * tabs
+            n += (2 if u.resident is not None else 3) * tabs
         return n
 
     def unit_args(self):
         return [(u.L, u.shards, u.master, u.m, u.v, u.grads, u.w.grad_stride,
-                 1.0 / u.w.n_ranks) for u in self.units]
+                 1.0 / u.w.n_ranks, u.resident) for u in self.units]
+
+    @staticmethod
+    def _update(u: Unit, hp: dict, t: int, stream):
+        z3.z3_reduce_scatter_adam(u.L, u.grads, u.w.grad_stride, 1.0 / u.w.n_ranks, None,
+                                  u.master, u.m, u.v, u.shards, hp, t, stream=stream)
+        if u.resident is not None:
+            z3.z3_allgather(u.L, u.shards, u.resident, stream=stream)
 
     def step(self, hp: dict, stream=None, t: int | None = None, on_gather=None):
         """One training step, scheduled by the library (z3_model_step).
@@ -96,16 +114,15 @@ class Model:
             z3.z3_model_step(self.unit_args(), [self.full], hp, t, stream=stream)
             return
         for i, u in enumerate(self.units):            # forward
-            z3.z3_allgather(u.L, u.shards, self.full, stream=stream)
-            if on_gather is not None:
-                on_gather("forward", i)
+            if u.resident is None:
+                z3.z3_allgather(u.L, u.shards, self.full, stream=stream)
+            on_gather("forward", i)
         for i in range(len(self.units) - 1, -1, -1):    # backward, reverse order
             u = self.units[i]
-            z3.z3_allgather(u.L, u.shards, self.full, stream=stream)
-            if on_gather is not None:
-                on_gather("backward", i)
-            z3.z3_reduce_scatter_adam(u.L, u.grads, u.w.grad_stride, 1.0 / u.w.n_ranks, None,
-                                      u.master, u.m, u.v, u.shards, hp, t, stream=stream)
+            if u.resident is None:
+                z3.z3_allgather(u.L, u.shards, self.full, stream=stream)
+            on_gather("backward", i)
+            self._update(u, hp, t, stream)
 
 
 def _torch_stream(stream):
@@ -156,19 +173,19 @@ class PrefetchModel(Model):
         freed = [torch.cuda.Event(), torch.cuda.Event()]
         g.wait_stream(main)                            # shards updated by the last step
         for i, u in enumerate(self.units):            # forward, back to back on g
-            z3.z3_allgather(u.L, u.shards, self.bufs[i % 2], stream=g.cuda_stream)
-            if on_gather is not None:
-                with torch.cuda.stream(g):
-                    on_gather("forward", i)
+            if u.resident is None:
+                z3.z3_allgather(u.L, u.shards, self.bufs[i % 2], stream=g.cuda_stream)
+            with torch.cuda.stream(g):
+                on_gather("forward", i)
         order = list(range(n - 1, -1, -1))
         gathered = {}
 
         def gather(i):
-            buf = self.bufs[i % 2]
-            z3.z3_allgather(self.units[i].L, self.units[i].shards, buf, stream=g.cuda_stream)
-            if on_gather is not None:
-                with torch.cuda.stream(g):
-                    on_gather("backward", i)
+            u = self.units[i]
+            if u.resident is None:
+                z3.z3_allgather(u.L, u.shards, self.bufs[i % 2], stream=g.cuda_stream)
+            with torch.cuda.stream(g):
+                on_gather("backward", i)
             ev = torch.cuda.Event()
             ev.record(g)
             gathered[i] = ev
@@ -181,14 +198,13 @@ class PrefetchModel(Model):
                     g.wait_event(freed[nxt % 2])       # buffer of unit i+1 is free again
                 gather(nxt)                            # prefetch one unit ahead
             main.wait_event(gathered[i])
-            z3.z3_reduce_scatter_adam(u.L, u.grads, u.w.grad_stride, 1.0 / u.w.n_ranks, None,
-                                      u.master, u.m, u.v, u.shards, hp, t,
-                                      stream=main.cuda_stream)
+            self._update(u, hp, t, main.cuda_stream)
             freed[i % 2].record(main)
         main.wait_stream(g)
 
 
-def full_step_model(dev, seed: int = 0, prefetch: int = 0, bucket_layers: int = 1) -> Model:
+def full_step_model(dev, seed: int = 0, prefetch: int = 0, bucket_layers: int = 1,
+                    persistence_threshold: int = 0) -> Model:
     """The 24-layer d=1024 model with its [50257, 1024] embedding, N_d = 16.
 
     bucket_layers: the parameter-bucket knob of "The ZeRO-3 Diagram Most
@@ -200,9 +216,14 @@ def full_step_model(dev, seed: int = 0, prefetch: int = 0, bucket_layers: int = 
 
     prefetch: how many units ahead the backward gathers run on a second stream
     (0: none; each unit of depth costs one more transient buffer).
+
+    persistence_threshold: the persistence-threshold knob of the same section
+    -- parameters of fewer elements are not released after use: they form
+    one resident unit whose gathered copy is kept and refreshed once per step
+    after its update, instead of being gathered before every use.
     """
     gen = I.make_generator(seed, dev)
-    units = [Unit(w, dev, gen) for w in I.full_step_units(bucket_layers)]
+    units = [Unit(w, dev, gen) for w in I.full_step_units(bucket_layers, persistence_threshold)]
     return PrefetchModel(units, dev, int(prefetch)) if prefetch else Model(units, dev)
 
 

@@ -161,3 +161,45 @@ def test_stage_and_reshard_entry_validation(lib):
     assert "different parameters" in z3.last_error()
     assert lib.z3_reshard(L.handle, L2.handle, 4, A, A + 16, None) == z3.Z3_ERR_INVALID_ARG
     assert lib.z3_reshard(L.handle, None, 4, A, far, None) == z3.Z3_ERR_INVALID_ARG
+
+
+def test_model_step_validation_without_gpu(lib):
+    """z3_model_step rejects bad unit lists, buffer counts, streams and
+    overlapping or misaligned buffers (resident copies included) before it
+    creates an event or launches anything (fake device addresses)."""
+    L = z3.Layout([35, 13, 12], 4)
+    A = 1 << 32
+    hp = z3.AdamHP(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    T = L.psi_padded
+
+    def unit(base, resident=None, layout=L):
+        # shards, master, m, v, grads laid out 1 MiB apart from base
+        a = [base + i * (1 << 20) for i in range(5)]
+        return z3.Unit(layout.handle.value if layout else None, a[0], a[1], a[2], a[3], a[4],
+                       64, 0.25, resident)
+
+    def call(units, fulls, n_full=None, gstream=None):
+        arr = (z3.Unit * len(units))(*units) if units else None
+        f = (ctypes.c_void_p * len(fulls))(*fulls)
+        return lib.z3_model_step(arr, len(units), f, len(fulls) if n_full is None else n_full,
+                                 ctypes.byref(hp), 1, None, gstream), z3.last_error()
+    full = A + (64 << 20)
+    s, msg = call([], [full])
+    assert s == z3.Z3_ERR_INVALID_ARG and "no units" in msg
+    s, msg = call([unit(A)], [full], n_full=0)
+    assert s == z3.Z3_ERR_INVALID_ARG
+    s, msg = call([unit(A)], [full] * 9)
+    assert s == z3.Z3_ERR_INVALID_ARG
+    s, msg = call([unit(A)], [full, full + (1 << 20)])           # prefetch without a stream
+    assert s == z3.Z3_ERR_INVALID_ARG and "gather stream" in msg
+    s, msg = call([unit(A, layout=None)], [full])
+    assert s == z3.Z3_ERR_INVALID_ARG and "layout" in msg
+    s, msg = call([unit(A)], [A + 16])                           # full overlaps shards
+    assert s == z3.Z3_ERR_INVALID_ARG and "overlaps" in msg
+    s, msg = call([unit(A, resident=A + (1 << 20))], [full])     # resident overlaps master
+    assert s == z3.Z3_ERR_INVALID_ARG and "overlaps" in msg
+    s, msg = call([unit(A, resident=A + (32 << 20) + 2)], [full])
+    assert s == z3.Z3_ERR_ALIGNMENT and "resident" in msg
+    s, msg = call([unit(A), unit(A + (8 << 20), resident=full + 16)], [full])
+    assert s == z3.Z3_ERR_INVALID_ARG and "overlaps" in msg      # resident inside full
+    assert T == 64

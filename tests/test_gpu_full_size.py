@@ -6,6 +6,8 @@ of outputs one by one from the input bytes read back at those positions:
 every rank's first and last owned element of every parameter, both sides of
 every pad boundary, and random positions.
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -365,3 +367,75 @@ def test_deeper_prefetch_matches(z3mod, depth):
         for k in ("master", "m", "v"):
             assert torch.equal(getattr(ua, k).view(torch.int32), getattr(ub, k).view(torch.int32))
         assert torch.equal(ua.shards.view(torch.int16), ub.shards.view(torch.int16))
+
+
+def _per_param(z3mod, model, ids, name):
+    """Every parameter's fp32 state (or, for name == "shards", its bf16
+    parameters) gathered to one rank, keyed by its model-order index."""
+    dev = torch.device("cuda")
+    out = {}
+    for u, pid in zip(model.units, ids):
+        buf = getattr(u, name)
+        dt = torch.float32 if buf.dtype == torch.float32 else torch.bfloat16
+        full = torch.empty(u.L.psi, dtype=dt, device=dev)
+        z3mod.z3_reshard(u.L, z3mod.Layout(u.w.numel, 1), buf, full)
+        a = 0
+        for i, n in zip(pid, u.w.numel):
+            out[i] = full[a:a + n]
+            a += n
+    return out
+
+
+@pytest.mark.parametrize("bucket,prefetch,threshold,issued", [
+    (1, 0, 100000, False), (4, 2, 100000, False), (2, 1, 100000, True), (1, 0, 100000, True),
+    (6, 1, 4194305, False), (1, 0, 10 ** 9, False)])
+def test_persistent_units_match_per_layer(z3mod, bucket, prefetch, threshold, issued):
+    """Persistence threshold: parameters below it form one resident unit that
+    is gathered once per step, after its update, and never released.  The
+    state after three steps equals the per-layer schedule's bit for bit, and
+    every resident copy holds exactly the current bf16 parameters."""
+    from optimizer_state_gb300 import schedule
+    dev = torch.device("cuda")
+    gen = I.make_generator(23, dev)
+    shapes = I._full_step_shapes()
+    numel = [math.prod(s) for s in shapes]
+    off = [0]
+    for n in numel:
+        off.append(off[-1] + n)
+    psi = off[-1]
+    master = torch.empty(psi, dtype=torch.float32, device=dev).normal_(0, 0.02, generator=gen)
+    grads = torch.empty((16, psi), dtype=torch.float32, device=dev).normal_(0, 1e-3,
+                                                                          generator=gen)
+    grads = grads.to(torch.bfloat16)
+
+    def build(b, T, depth):
+        ws, ids = I.full_step_units(b, T), I.full_step_param_ids(b, T)
+        units = []
+        for w, pid in zip(ws, ids):
+            mf = torch.cat([master[off[i]:off[i + 1]] for i in pid])
+            gf = torch.cat([grads[:, off[i]:off[i + 1]] for i in pid], dim=1)
+            units.append(schedule.Unit.from_full(w, dev, mf, gf))
+        model = schedule.PrefetchModel(units, dev, depth) if depth else schedule.Model(units, dev)
+        return model, ids
+    ref, ref_ids = build(1, 0, 0)
+    mp, ids = build(bucket, threshold, prefetch)
+    assert mp.units[0].resident is not None
+    for _ in range(3):
+        ref.step(HP)
+        if issued:
+            mp.step(HP, on_gather=lambda phase, i: None)
+        else:
+            mp.step(HP)
+    torch.cuda.synchronize()
+    for name in ("master", "m", "v", "shards"):
+        a, b = _per_param(z3mod, ref, ref_ids, name), _per_param(z3mod, mp, ids, name)
+        vt = torch.int16 if name == "shards" else torch.int32
+        for i in range(len(shapes)):
+            assert torch.equal(a[i].view(vt), b[i].view(vt)), (name, i)
+    bf = _per_param(z3mod, mp, ids, "shards")
+    u0 = mp.units[0]
+    want = torch.cat([bf[i] for i in ids[0]])
+    assert torch.equal(u0.resident.view(torch.int16), want.view(torch.int16))
+    assert torch.equal(want.view(torch.int16),
+                       torch.cat([_per_param(z3mod, mp, ids, "master")[i] for i in ids[0]])
+                       .to(torch.bfloat16).view(torch.int16))
