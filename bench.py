@@ -303,7 +303,7 @@ def run_cuda(args, world, rank, local):
             "pct_of_8tbs": round(100.0 * value / (NOMINAL_HBM_GBS * world), 2),
             "kernels_ms": {"allgather": round(t_ag, 6), "reduce_scatter_adam": round(t_rs, 6)},
             "roofline": {
-                "kernel": "k_reduce_aligned<RSAdam> (fused reduce-scatter + Adam)",
+                "kernel": f"{reduce_kernel_name(L)}<RSAdam> (fused reduce-scatter + Adam)",
                 "bound": "hbm",
                 "achieved": round(achieved, 2),
                 "peak": peak,
@@ -325,7 +325,8 @@ def run_cuda(args, world, rank, local):
         dist.destroy_process_group()
 
 
-LAYER_WORKLOADS = ("layer_d1024_nd8", "layer_7b_nd8", "layer_7b_nd64", "layer_primes_nd8")
+LAYER_WORKLOADS = ("layer_d1024_nd8", "layer_7b_nd8", "layer_7b_nd64", "layer_primes_nd8",
+                   "layer_primes_small_nd8")
 
 
 def layer_workload(name: str):
@@ -336,7 +337,19 @@ def layer_workload(name: str):
         return I.layer_7b(int(name[len("layer_7b_nd"):]))
     if name.startswith("layer_primes_nd"):
         return I.layer_primes(int(name[len("layer_primes_nd"):]))
+    if name.startswith("layer_primes_small_nd"):
+        return I.layer_primes(int(name[len("layer_primes_small_nd"):]), small=True)
     raise SystemExit(f"unknown layer workload {name}")
+
+
+def reduce_kernel_name(L) -> str:
+    """The reduce kernel a layer's launch runs: the aligned one when every
+    (parameter, rank) chunk's full-space and shard-space indices agree modulo
+    the 8-element vector, else the window-shifting one."""
+    aligned = all((F + r * s - (r * L.S + o)) % 8 == 0
+                  for n, s, o, F in zip(L.numel, L.shard_numel, L.shard_off, L.full_off) if n
+                  for r in range(L.n_ranks))
+    return "k_reduce_aligned" if aligned else "k_reduce_shifted"
 
 
 def len_tabs(L, kind):
@@ -444,6 +457,22 @@ def run_multi(args, world, rank, local):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
+    graph = None
+    if args.graph:
+        # the K timed steps (step counter advancing) captured as one CUDA
+        # graph, replayed once inside the timed region: no host launch cost
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap), torch.cuda.graph(graph, stream=cap):
+            sid_saved = sid
+            sid = cap.cuda_stream
+            for i in range(args.steps):
+                step(args.warmup + i)
+            sid = sid_saved
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+        extra["launch"] = f"one CUDA graph of the {args.steps} timed steps"
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -453,8 +482,11 @@ def run_multi(args, world, rank, local):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks.mark(True)
     e0.record(stream)
-    for i in range(args.steps):
-        step(args.warmup + i)
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(args.steps):
+            step(args.warmup + i)
     e1.record(stream)
     torch.cuda.synchronize()
     clocks.mark(False)
@@ -743,6 +775,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-seconds", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="full-step and sweep workloads: replay the timed steps as one CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

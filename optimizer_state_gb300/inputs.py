@@ -82,10 +82,15 @@ def layer_7b(n_ranks: int) -> Workload:
                     n_ranks=n_ranks, param_std=0.02, grad_std=1e-3)
 
 
-def layer_primes(n_ranks: int) -> Workload:
+def layer_primes(n_ranks: int, small: bool = False) -> Workload:
     """A layer of three prime-length parameters: every chunk after the first
     has a different phase between its full-space and shard-space indices,
-    so the reduce and gather kernels must shift 16-byte windows."""
+    so the reduce and gather kernels must shift 16-byte windows.  The small
+    variant (13.6 M elements, its gradients still larger than L2) is the
+    profiling case of the same kernels."""
+    if small:
+        return Workload(f"layer_primes_small_nd{n_ranks}", ((8388617,), (4194319,), (1048583,)),
+                        n_ranks=n_ranks, param_std=0.02, grad_std=1e-3)
     return Workload(f"layer_primes_nd{n_ranks}", ((67108879,), (33554467,), (1048583,)),
                     n_ranks=n_ranks, param_std=0.02, grad_std=1e-3)
 

@@ -70,3 +70,40 @@ def test_side_stream(mods):
     s.synchronize()
     torch.cuda.synchronize()
     assert np.array_equal(bits32(f32(a.master)), bits32(f32(b.master)))
+
+
+@pytest.mark.parametrize("depth", [0, 2])
+def test_captured_model_step_equals_eager(mods, depth):
+    """A whole model step (z3_model_step: the units' gathers, updates and,
+    with prefetch, the fork onto the gather stream and the join back) with
+    a resident unit, captured once and replayed twice, equals two eager
+    steps at the same t, bit for bit."""
+    z3, sch = mods
+    dev = torch.device("cuda")
+    ws = [I.Workload("res", ((77,), (1024,)), 8, 0.02, 1e-3, resident=True),
+          I.Workload("u1", ((100003,), (4099,)), 8, 0.02, 1e-3),
+          I.Workload("u2", ((65536,), (3, 1001)), 8, 0.02, 1e-3),
+          I.Workload("u3", ((262147,),), 8, 0.02, 1e-3)]
+
+    def model(seed):
+        gen = I.make_generator(seed, dev)
+        units = [sch.Unit(w, dev, gen) for w in ws]
+        return sch.PrefetchModel(units, dev, depth) if depth else sch.Model(units, dev)
+    a, b = model(9), model(9)
+    for _ in range(2):
+        a.step(HP, t=1)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s), torch.cuda.graph(g, stream=s):
+        b.step(HP, stream=s.cuda_stream, t=1)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for ua, ub in zip(a.units, b.units):
+        for k in ("master", "m", "v"):
+            assert np.array_equal(bits32(f32(getattr(ua, k))), bits32(f32(getattr(ub, k)))), k
+        assert np.array_equal(u16(ua.shards), u16(ub.shards))
+    assert np.array_equal(u16(a.units[0].resident), u16(b.units[0].resident))
