@@ -458,6 +458,8 @@ def run_multi(args, world, rank, local):
         step(i)
     torch.cuda.synchronize()
     graph = None
+    if args.graph and launches * args.steps > 50000:
+        raise SystemExit(f"--graph: {launches * args.steps} launches in one graph; use fewer --steps")
     if args.graph:
         # the K timed steps (step counter advancing) captured as one CUDA
         # graph, replayed once inside the timed region: no host launch cost
