@@ -275,3 +275,50 @@ def test_wide_gradient_pitch_and_late_steps(z3mod, orc):
     k = orc.adam_constants(HP["lr"], HP["beta1"], HP["beta2"], HP["eps"], 0.0, 10 ** 6)
     assert k["rb1"] == 1.0 and k["rb2"] == 1.0
     assert c.guards_ok()
+
+
+@pytest.mark.parametrize("depth", [0, 1, 2])
+def test_model_step_matches_oracle(z3mod, orc, depth):
+    """z3_model_step over four units (one resident, odd lengths, N_d = 5),
+    three steps, with 0, 1 and 2 units of gather prefetch: every unit's
+    state equals the oracle's layer step bit for bit, the resident copy
+    equals the oracle's gather of the updated shards, each transient buffer
+    holds the backward gather of the last unit that used it, and no call
+    writes outside its buffers."""
+    N = 5
+    specs = [([77, 1024, 5], True), ([100003, 7], False), ([4099, 65536, 1], False),
+             ([262147], False)]
+    cases = [Case(z3mod, orc, numel, N, seed=40 + i) for i, (numel, _) in enumerate(specs)]
+    resident = [Guarded(c.L.psi, torch.bfloat16) if res else None
+                for c, (_, res) in zip(cases, specs)]
+    for c, r in zip(cases, resident):
+        if r is not None:
+            z3mod.z3_allgather(c.L, c.shards.t, r.t)
+    nb = depth + 1
+    big = max(c.L.psi for c, (_, res) in zip(cases, specs) if not res)
+    fulls = [Guarded(big, torch.bfloat16) for _ in range(nb)]
+    gstream = torch.cuda.Stream() if depth else None
+    scale = 1.0 / N
+    for t in (1, 2, 3):
+        drawn = [c.grads() for c in cases]
+        units = [(c.L, c.shards.t, c.master.t, c.m.t, c.v.t, g, c.stride, scale,
+                  None if r is None else r.t) for c, (g, _), r in zip(cases, drawn, resident)]
+        z3mod.z3_model_step(units, [f.t for f in fulls], HP, t, gather_stream=gstream)
+        last_bwd = {}
+        for i in range(len(cases) - 1, -1, -1):      # backward order
+            c, (_, gh) = cases[i], drawn[i]
+            _, fb, _ = orc.step_layer(c.O, c.o["shards"], gh, c.stride, scale, c.o["master"],
+                                      c.o["m"], c.o["v"], HP, t)
+            if resident[i] is None:
+                last_bwd[i % nb] = fb
+        torch.cuda.synchronize()
+        for c in cases:
+            assert_adam_equal(c.device_state(), c.o)
+            assert c.guards_ok()
+        for c, r in zip(cases, resident):
+            if r is not None:
+                assert np.array_equal(u16(r.t), orc.allgather(c.O, c.o["shards"]))
+                assert r.guards_intact()
+        for b, fb in last_bwd.items():
+            assert np.array_equal(u16(fulls[b].t)[:fb.size], fb), f"buffer {b}"
+        assert all(f.guards_intact() for f in fulls)
