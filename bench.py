@@ -573,12 +573,12 @@ def run_kernels(args, local):
 
 
 def run_e2e(args, z3, L, w, rep, stream, sid, step_bytes, world):
-    """The same step through the public API with host buffers.  Every step
-    uploads its gradients host->device from pinned memory and reads the
-    updated bf16 shards back device->host, inside the timed region.  The
-    upload of step i+1 (into a second gradient buffer) runs on a copy stream
-    while step i computes and its result is read back; a step's update waits
-    for the previous read-back, so no copy ever sees a half-written buffer."""
+    """The same step through the C ABI with host buffers (z3_host_step_run):
+    every step uploads its gradients from page-locked host memory into one of
+    two device staging buffers and reads the updated bf16 shards back into
+    host memory, inside the timed region.  The library overlaps the upload
+    of step i+1 with the compute and read-back of step i, ordering every
+    buffer reuse with CUDA events."""
     import torch
     k = max(3, min(args.steps, args.e2e_steps))
     host_grads = torch.empty(rep.grads.shape, dtype=rep.grads.dtype, pin_memory=True)
@@ -586,46 +586,21 @@ def run_e2e(args, z3, L, w, rep, stream, sid, step_bytes, world):
     host_out = torch.empty(rep.shards.shape, dtype=rep.shards.dtype, pin_memory=True)
     h2d = host_grads.numel() * host_grads.element_size()
     d2h = host_out.numel() * host_out.element_size()
-    bufs = [rep.grads, torch.empty_like(rep.grads)]
+    staging = [rep.grads, torch.empty_like(rep.grads)]
     up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    pipe = z3.HostStep(L, staging[0], staging[1], w.grad_stride, up, down)
 
     def run(n):
-        read = None                     # read-back of the previous step done
-        done = [None, None]             # compute finished with gradient buffer b
-
-        def upload(i):
-            b = i % 2
-            if done[b] is not None:
-                up.wait_event(done[b])  # step i-2 no longer reads this buffer
-            with torch.cuda.stream(up):
-                bufs[b].copy_(host_grads, non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record(up)
-            return ev
-        arrived = {0: upload(0)}
-        for i in range(n):
-            b = i % 2
-            if i + 1 < n:
-                arrived[i + 1] = upload(i + 1)   # overlaps step i
-            stream.wait_event(arrived[i])
-            if read is not None:
-                stream.wait_event(read)          # step i-1's shards have been read back
+        for _ in range(n):
             rep.step += 1
-            z3.z3_step_layer(L, rep.shards, rep.full, bufs[b], w.grad_stride, 1.0 / w.n_ranks,
-                             rep.master, rep.m, rep.v, HP, rep.step, stream=sid)
-            ev = torch.cuda.Event()
-            ev.record(stream)
-            done[b] = ev
-            down.wait_event(ev)
-            with torch.cuda.stream(down):
-                host_out.copy_(rep.shards, non_blocking=True)
-            read = torch.cuda.Event()
-            read.record(down)
-        stream.wait_stream(down)
+            pipe.run(host_grads, rep.shards, rep.full, 1.0 / w.n_ranks, rep.master, rep.m,
+                     rep.v, HP, rep.step, shards_host=host_out, stream=sid)
+        stream.wait_stream(down)                 # the last read-back is part of the step
         stream.wait_stream(up)
     run(2)
     torch.cuda.synchronize()
-    link = host_link_h2d_gbs(host_grads, bufs[1], up)
+    link = host_link_h2d_gbs(host_grads, staging[1], up)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -634,6 +609,7 @@ def run_e2e(args, z3, L, w, rep, stream, sid, step_bytes, world):
     run(k)
     e1.record(stream)
     torch.cuda.synchronize()
+    pipe.close()
     ms = e0.elapsed_time(e1)
     value = world * step_bytes * k / (ms * 1e-3) / 1e9
     # no step can finish faster than its upload: step bytes / (upload bytes / link rate)
@@ -641,6 +617,7 @@ def run_e2e(args, z3, L, w, rep, stream, sid, step_bytes, world):
     return {"value": round(value, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k,
             "ms_per_step": round(ms / k, 6),
+            "api": "z3_host_step_run (C ABI, pinned host buffers)",
             "pipeline": "upload of step i+1 overlaps compute and read-back of step i",
             "host_link_h2d_gbs": round(link, 1), "upload_bound": round(bound, 2),
             "frac_of_upload_bound": round(value / bound, 4)}

@@ -243,6 +243,51 @@ z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16_t *const *
                         int32_t n_full, const z3_adam_hp *hp, int64_t step,
                         z3_stream stream, z3_stream gather_stream);
 
+/* ---- the layer step fed from host memory ------------------------------- */
+
+/* A pipeline that runs z3_step_layer on gradients held in host memory and
+ * returns the updated bf16 parameters to host memory: each call uploads the
+ * N ranks' gradients into one of two device staging buffers, runs the layer
+ * step ([ZD] s.3: AllGather, AllGather, ReduceScatter + the shard update)
+ * from that buffer, and downloads the updated shards.  Consecutive calls
+ * alternate the staging buffers, so the upload of call i+1 (on
+ * upload_stream) overlaps the compute of call i (on the call's stream) and
+ * the download of call i (on download_stream).  CUDA events order every
+ * reuse: an upload into a staging buffer waits for the step that last read
+ * it; a step waits for its upload and for the previous call's download (the
+ * step rewrites the shards that download reads); a download waits for its
+ * step.
+ *
+ * Ownership: the caller owns the two staging buffers (device, bf16
+ * [N][grad_stride] each, 16-byte aligned, not overlapping) and both streams;
+ * the pipeline owns only its CUDA events (created here, destroyed by
+ * z3_host_step_destroy).  A pipeline belongs to one layout and one calling
+ * thread at a time.  Errors: NULL layout, staging buffer or stream, equal
+ * streams, misaligned or overlapping staging buffers, grad_stride as for
+ * z3_reduce_scatter (INVALID_ARG / ALIGNMENT); event creation failing
+ * (CUDA). */
+typedef struct z3_host_step z3_host_step;
+
+z3_status z3_host_step_create(const z3_layout *layout, uint16_t *staging0,
+                              uint16_t *staging1, int64_t grad_stride,
+                              z3_stream upload_stream, z3_stream download_stream,
+                              z3_host_step **out);
+
+/* One layer step from host memory.  grads_host: bf16 [N][grad_stride] in
+ * host memory, read by the upload (page-locked memory lets the copy run
+ * asynchronously; the caller keeps it unchanged until the call's stream has
+ * passed this step).  shards_host: bf16 [N][S] host memory written by the
+ * download, or NULL for no download.  The device state arguments and the
+ * errors are those of z3_step_layer; stream must differ from both pipeline
+ * streams. */
+z3_status z3_host_step_run(z3_host_step *pipe, const uint16_t *grads_host,
+                           uint16_t *shards, uint16_t *full, float scale,
+                           float *master, float *m, float *v,
+                           const z3_adam_hp *hp, int64_t step,
+                           uint16_t *shards_host, z3_stream stream);
+
+void z3_host_step_destroy(z3_host_step *pipe);
+
 /* ---- stage 1 / stage 2 / plain data-parallel variants ------------------ */
 
 /* Plain data-parallel all-reduce ([S3] communication list: the baseline's

@@ -7,6 +7,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <new>
 #include <cstdint>
 #include <string>
 #include <vector>
@@ -219,6 +220,23 @@ z3_status prepare_rs_adam(const char *fn, const z3_layout *L, const uint16_t *gr
     a->shards = shards;
     return Z3_OK;
 }
+// forward AllGather, backward AllGather, then ReduceScatter + Adam
+z3_status enqueue_step_layer(const char *fn, const z3_layout *L, const ReduceArgs &a,
+                             uint16_t *shards, uint16_t *full, cudaStream_t s) {
+    z3_status st;
+    {
+        Range r1("z3/AllGather(forward)");
+        st = run_allgather(L, shards, full, s);
+    }
+    if (st != Z3_OK) return st;
+    {
+        Range r2("z3/AllGather(backward)");
+        st = run_allgather(L, shards, full, s);
+    }
+    if (st != Z3_OK) return st;
+    Range r3("z3/ReduceScatter+Adam");
+    return run_reduce(L, a, kRSAdam, s, fn);
+}
 }  // namespace
 
 extern "C" z3_status z3_reduce_scatter_adam(const z3_layout *L, const uint16_t *grads,
@@ -246,21 +264,8 @@ extern "C" z3_status z3_step_layer(const z3_layout *L, uint16_t *shards, uint16_
                                    shards, full, hp, step, &a);
     if (st != Z3_OK) return st;
     if (L->psi_padded == 0) return Z3_OK;
-    const cudaStream_t s = (cudaStream_t)stream;
     Range range("z3/step_layer");
-    // forward AllGather, backward AllGather, then ReduceScatter + Adam
-    {
-        Range r1("z3/AllGather(forward)");
-        st = run_allgather(L, shards, full, s);
-    }
-    if (st != Z3_OK) return st;
-    {
-        Range r2("z3/AllGather(backward)");
-        st = run_allgather(L, shards, full, s);
-    }
-    if (st != Z3_OK) return st;
-    Range r3("z3/ReduceScatter+Adam");
-    return run_reduce(L, a, kRSAdam, s, fn);
+    return enqueue_step_layer(fn, L, a, shards, full, (cudaStream_t)stream);
 }
 
 extern "C" z3_status z3_allreduce(const z3_layout *L, const uint16_t *grads, int64_t grad_stride,
@@ -465,3 +470,125 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
     if ((err = cudaStreamWaitEvent(s, E.ev[1], 0)) != cudaSuccess) return cuda_fail(err);
     return Z3_OK;
 }
+
+// --------------------------------------------------------------------------
+// the layer step fed from host memory
+// --------------------------------------------------------------------------
+
+struct z3_host_step {
+    const z3_layout *L = nullptr;
+    uint16_t *staging[2] = {nullptr, nullptr};
+    int64_t stride = 0;
+    int64_t grad_bytes = 0;
+    cudaStream_t up = nullptr, down = nullptr;
+    cudaEvent_t done[2] = {nullptr, nullptr};  // the step that last read staging[b] has run
+    cudaEvent_t uploaded = nullptr;            // this call's upload has landed
+    cudaEvent_t read = nullptr;                // the last download has finished
+    bool done_valid[2] = {false, false};
+    bool read_valid = false;
+    int64_t calls = 0;
+
+    ~z3_host_step() {
+        for (cudaEvent_t e : {done[0], done[1], uploaded, read})
+            if (e != nullptr) cudaEventDestroy(e);
+    }
+};
+
+extern "C" z3_status z3_host_step_create(const z3_layout *L, uint16_t *staging0,
+                                         uint16_t *staging1, int64_t grad_stride,
+                                         z3_stream upload_stream, z3_stream download_stream,
+                                         z3_host_step **out) {
+    const char *fn = "z3_host_step_create";
+    if (out == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_host_step_create: out is NULL");
+    *out = nullptr;
+    if (L == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_host_step_create: layout is NULL");
+    if (upload_stream == nullptr || download_stream == nullptr || upload_stream == download_stream)
+        return fail(Z3_ERR_INVALID_ARG,
+                    "z3_host_step_create: upload and download streams must be two distinct "
+                    "non-NULL streams");
+    int64_t gbytes;
+    z3_status st = check_grads(fn, L, grad_stride, &gbytes);
+    if (st != Z3_OK) return st;
+    // a zero-element layer still needs two distinct staging pointers
+    const int64_t b = gbytes > 0 ? gbytes : 16;
+    const Buf bufs[2] = {{staging0, b, "staging0"}, {staging1, b, "staging1"}};
+    st = check_bufs(fn, bufs, 2);
+    if (st != Z3_OK) return st;
+    auto *p = new (std::nothrow) z3_host_step();
+    if (p == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_host_step_create: out of host memory");
+    p->L = L;
+    p->staging[0] = staging0;
+    p->staging[1] = staging1;
+    p->stride = grad_stride;
+    p->grad_bytes = gbytes;
+    p->up = (cudaStream_t)upload_stream;
+    p->down = (cudaStream_t)download_stream;
+    for (cudaEvent_t *e : {&p->done[0], &p->done[1], &p->uploaded, &p->read}) {
+        const cudaError_t err = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
+        if (err != cudaSuccess) {
+            delete p;
+            return launched(fn, err);
+        }
+    }
+    *out = p;
+    return Z3_OK;
+}
+
+extern "C" z3_status z3_host_step_run(z3_host_step *p, const uint16_t *grads_host,
+                                      uint16_t *shards, uint16_t *full, float scale,
+                                      float *master, float *m, float *v, const z3_adam_hp *hp,
+                                      int64_t step, uint16_t *shards_host, z3_stream stream) {
+    const char *fn = "z3_host_step_run";
+    if (p == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_host_step_run: pipeline is NULL");
+    const cudaStream_t s = (cudaStream_t)stream;
+    if (s == p->up || s == p->down)
+        return fail(Z3_ERR_INVALID_ARG,
+                    "z3_host_step_run: stream must differ from the pipeline's streams");
+    const z3_layout *L = p->L;
+    const int b = (int)(p->calls & 1);
+    ReduceArgs a{};
+    z3_status st = prepare_rs_adam(fn, L, p->staging[b], p->stride, scale, nullptr, master, m,
+                                   v, shards, full, hp, step, &a);
+    if (st != Z3_OK) return st;
+    const int64_t T = L->psi_padded;
+    const Buf dev[2] = {{p->staging[1 - b], p->grad_bytes, "the other staging buffer"},
+                        {shards, 2 * T, "shards"}};
+    st = check_bufs(fn, dev, 2);
+    if (st != Z3_OK) return st;
+    if (p->grad_bytes > 0 && grads_host == nullptr)
+        return fail(Z3_ERR_INVALID_ARG, "z3_host_step_run: grads_host is NULL");
+    Range range("z3/host_step");
+    cudaError_t err = cudaSuccess;
+    auto ok = [&](cudaError_t e) { err = e; return e == cudaSuccess; };
+    // upload into staging[b] once the step that last read it has run
+    if (p->done_valid[b] && !ok(cudaStreamWaitEvent(p->up, p->done[b], 0))) return launched(fn, err);
+    if (p->grad_bytes > 0) {
+        Range r("z3/upload gradients");
+        if (!ok(cudaMemcpyAsync(p->staging[b], grads_host, (size_t)p->grad_bytes,
+                                cudaMemcpyHostToDevice, p->up)))
+            return launched(fn, err);
+    }
+    if (!ok(cudaEventRecord(p->uploaded, p->up))) return launched(fn, err);
+    // the step: after its upload, and after the previous download of the shards it rewrites
+    if (!ok(cudaStreamWaitEvent(s, p->uploaded, 0))) return launched(fn, err);
+    if (p->read_valid && !ok(cudaStreamWaitEvent(s, p->read, 0))) return launched(fn, err);
+    if (T > 0) {
+        st = enqueue_step_layer(fn, L, a, shards, full, s);
+        if (st != Z3_OK) return st;
+    }
+    if (!ok(cudaEventRecord(p->done[b], s))) return launched(fn, err);
+    p->done_valid[b] = true;
+    p->calls += 1;
+    if (shards_host != nullptr && T > 0) {
+        Range r("z3/download parameters");
+        if (!ok(cudaStreamWaitEvent(p->down, p->done[b], 0))) return launched(fn, err);
+        if (!ok(cudaMemcpyAsync(shards_host, shards, (size_t)(2 * T), cudaMemcpyDeviceToHost,
+                                p->down)))
+            return launched(fn, err);
+        if (!ok(cudaEventRecord(p->read, p->down))) return launched(fn, err);
+        p->read_valid = true;
+    }
+    return Z3_OK;
+}
+
+extern "C" void z3_host_step_destroy(z3_host_step *p) { delete p; }

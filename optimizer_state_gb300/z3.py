@@ -26,6 +26,7 @@ EXPORTS = ("z3_layout_create", "z3_layout_destroy", "z3_layout_info", "z3_layout
            "z3_stats", "z3_partition", "z3_allgather", "z3_reduce_scatter",
            "z3_adam_shard_step", "z3_reduce_scatter_adam", "z3_step_layer",
            "z3_allreduce", "z3_scatter", "z3_reshard", "z3_model_step",
+           "z3_host_step_create", "z3_host_step_run", "z3_host_step_destroy",
            "z3_status_string", "z3_last_error")
 
 
@@ -95,6 +96,9 @@ def load():
             "z3_reshard": (st, [vp, vp, i32, vp, vp, vp]),
             "z3_model_step": (st, [ctypes.POINTER(Unit), i32, ctypes.POINTER(vp), i32, hp, i64,
                                    vp, vp]),
+            "z3_host_step_create": (st, [vp, vp, vp, i64, vp, vp, ctypes.POINTER(vp)]),
+            "z3_host_step_run": (st, [vp, vp, vp, vp, f32, vp, vp, vp, hp, i64, vp, vp]),
+            "z3_host_step_destroy": (None, [vp]),
             "z3_status_string": (ctypes.c_char_p, [st]),
             "z3_last_error": (ctypes.c_size_t, [ctypes.c_char_p, ctypes.c_size_t]),
         }
@@ -313,3 +317,61 @@ def z3_model_step(units, full, hp, step: int, stream=None, gather_stream=None):
     _check(load().z3_model_step(arr, len(units), fulls, len(full), ctypes.byref(h), step,
                                 _stream(stream),
                                 None if gather_stream is None else _stream(gather_stream)))
+
+
+def _host(t, dtypes, numel: int, name: str):
+    """Host address of a CPU tensor (or a raw int address)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if t.is_cuda:
+        raise ValueError(f"{name}: must be a host (CPU) tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: needs >= {numel} elements, has {t.numel()}")
+    return t.data_ptr()
+
+
+class HostStep:
+    """z3_host_step_create / _run / _destroy: the layer step fed from host
+    memory through two device staging buffers (caller-owned tensors kept
+    alive by this object)."""
+
+    def __init__(self, layout: Layout, staging0, staging1, grad_stride: int, upload_stream,
+                 download_stream):
+        b16, _ = _dtypes()
+        n = layout.n_ranks * grad_stride
+        self._keep = (layout, staging0, staging1, upload_stream, download_stream)
+        self.layout, self.grad_stride = layout, grad_stride
+        h = ctypes.c_void_p()
+        _check(load().z3_host_step_create(
+            layout.handle, _dev(staging0, b16, n, "staging0"), _dev(staging1, b16, n, "staging1"),
+            grad_stride, _stream(upload_stream), _stream(download_stream), ctypes.byref(h)))
+        self._h = h
+
+    def run(self, grads_host, shards, full, scale: float, master, m, v, hp, step: int,
+            shards_host=None, stream=None):
+        b16, f32 = _dtypes()
+        L = self.layout
+        T = L.psi_padded
+        h = _hp(hp)
+        _check(load().z3_host_step_run(
+            self._h, _host(grads_host, b16, L.n_ranks * self.grad_stride, "grads_host"),
+            _dev(shards, b16, T, "shards"), _dev(full, b16, L.psi, "full"), scale,
+            _dev(master, f32, T, "master"), _dev(m, f32, T, "m"), _dev(v, f32, T, "v"),
+            ctypes.byref(h), step, _host(shards_host, b16, T, "shards_host"), _stream(stream)))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            load().z3_host_step_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001 - interpreter shutdown
+            pass

@@ -203,3 +203,40 @@ def test_model_step_validation_without_gpu(lib):
     s, msg = call([unit(A), unit(A + (8 << 20), resident=full + 16)], [full])
     assert s == z3.Z3_ERR_INVALID_ARG and "overlaps" in msg      # resident inside full
     assert T == 64
+
+
+def test_host_step_validation_without_gpu(lib):
+    """z3_host_step_create rejects bad layouts, streams and staging buffers
+    before it creates any CUDA object (fake addresses and stream handles)."""
+    L = z3.Layout([35, 13, 12], 4)
+    A = 1 << 32
+    far = A + (1 << 28)
+    up, down = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000)
+    h = ctypes.c_void_p()
+
+    def create(layout, s0, s1, stride, u, d, out=True):
+        st = lib.z3_host_step_create(layout, s0, s1, stride, u, d,
+                                     ctypes.byref(h) if out else None)
+        return st, z3.last_error()
+    s, msg = create(L.handle, A, far, 64, up, down, out=False)
+    assert s == z3.Z3_ERR_INVALID_ARG and "out" in msg
+    s, msg = create(None, A, far, 64, up, down)
+    assert s == z3.Z3_ERR_INVALID_ARG and "layout" in msg
+    s, msg = create(L.handle, A, far, 64, None, down)
+    assert s == z3.Z3_ERR_INVALID_ARG and "stream" in msg
+    s, msg = create(L.handle, A, far, 64, up, up)
+    assert s == z3.Z3_ERR_INVALID_ARG and "stream" in msg
+    s, msg = create(L.handle, A, far, 59, up, down)
+    assert s == z3.Z3_ERR_INVALID_ARG and "grad_stride" in msg
+    s, msg = create(L.handle, A, far, 68, up, down)
+    assert s == z3.Z3_ERR_ALIGNMENT
+    s, msg = create(L.handle, A, None, 64, up, down)
+    assert s == z3.Z3_ERR_INVALID_ARG and "staging1" in msg
+    s, msg = create(L.handle, A + 8, far, 64, up, down)
+    assert s == z3.Z3_ERR_ALIGNMENT and "staging0" in msg
+    s, msg = create(L.handle, A, A + 64, 64, up, down)       # 4 ranks x 64 x 2 B = 512 B
+    assert s == z3.Z3_ERR_INVALID_ARG and "overlaps" in msg
+    assert h.value is None
+    assert lib.z3_host_step_run(None, A, A, A, 0.25, A, A, A, None, 1, None, None) == \
+        z3.Z3_ERR_INVALID_ARG
+    lib.z3_host_step_destroy(None)                           # a no-op
