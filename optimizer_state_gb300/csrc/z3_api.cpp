@@ -97,14 +97,17 @@ struct Range {
     Range &operator=(const Range &) = delete;
 };
 
+// early: see launch_allgather / launch_reduce.  Only the calls that enqueue
+// several dependent launches pass true, for a launch whose stream
+// predecessor they enqueued themselves.
 z3_status run_allgather(const z3_layout *L, const uint16_t *shards, uint16_t *full,
-                        cudaStream_t stream) {
-    return launched("z3_allgather", launch_allgather(L, shards, full, stream));
+                        cudaStream_t stream, bool early = false) {
+    return launched("z3_allgather", launch_allgather(L, shards, full, stream, early));
 }
 
 z3_status run_reduce(const z3_layout *L, const ReduceArgs &a, Mode mode, cudaStream_t stream,
-                     const char *fn) {
-    return launched(fn, launch_reduce(L, a, mode, stream));
+                     const char *fn, bool early = false) {
+    return launched(fn, launch_reduce(L, a, mode, stream, early));
 }
 
 }  // namespace
@@ -220,7 +223,10 @@ z3_status prepare_rs_adam(const char *fn, const z3_layout *L, const uint16_t *gr
     a->shards = shards;
     return Z3_OK;
 }
-// forward AllGather, backward AllGather, then ReduceScatter + Adam
+// forward AllGather, backward AllGather, then ReduceScatter + Adam.  The
+// backward gather's predecessor (the forward gather) writes only `full`, so
+// it reads the shards early; the update's predecessor (the backward gather)
+// writes only `full`, so it reads gradients and state early.
 z3_status enqueue_step_layer(const char *fn, const z3_layout *L, const ReduceArgs &a,
                              uint16_t *shards, uint16_t *full, cudaStream_t s) {
     z3_status st;
@@ -231,11 +237,11 @@ z3_status enqueue_step_layer(const char *fn, const z3_layout *L, const ReduceArg
     if (st != Z3_OK) return st;
     {
         Range r2("z3/AllGather(backward)");
-        st = run_allgather(L, shards, full, s);
+        st = run_allgather(L, shards, full, s, true);
     }
     if (st != Z3_OK) return st;
     Range r3("z3/ReduceScatter+Adam");
-    return run_reduce(L, a, kRSAdam, s, fn);
+    return run_reduce(L, a, kRSAdam, s, fn, true);
 }
 }  // namespace
 
@@ -382,34 +388,84 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
             }
         }
     }
+    // The units' written buffers must be disjoint from every buffer of every
+    // other unit: a launch then never reads what its stream predecessor (a
+    // launch of another unit, or of this unit's gather) writes, which lets
+    // the gathers read shards and the updates read gradients and state
+    // before they wait for that predecessor.
+    for (int32_t i = 0; i < n_units; ++i) {
+        const z3_unit &u = units[i];
+        const int64_t T = u.layout->psi_padded;
+        for (int32_t j = i + 1; j < n_units; ++j) {
+            const z3_unit &w = units[j];
+            const int64_t Tw = w.layout->psi_padded;
+            int64_t gu = 0, gw = 0;
+            check_grads(fn, u.layout, u.grad_stride, &gu);
+            check_grads(fn, w.layout, w.grad_stride, &gw);
+            const Buf mine[5] = {{u.shards, 2 * T, "a unit's shards"},
+                                 {u.master, 4 * T, "a unit's master"},
+                                 {u.m, 4 * T, "a unit's m"},
+                                 {u.v, 4 * T, "a unit's v"},
+                                 {u.resident, u.resident ? 2 * u.layout->psi : 0,
+                                  "a unit's resident copy"}};
+            const Buf theirs[6] = {{w.shards, 2 * Tw, "another unit's shards"},
+                                   {w.master, 4 * Tw, "another unit's master"},
+                                   {w.m, 4 * Tw, "another unit's m"},
+                                   {w.v, 4 * Tw, "another unit's v"},
+                                   {w.resident, w.resident ? 2 * w.layout->psi : 0,
+                                    "another unit's resident copy"},
+                                   {w.grads, w.layout->psi ? gw : 0, "another unit's grads"}};
+            const Buf their_w[5] = {theirs[0], theirs[1], theirs[2], theirs[3], theirs[4]};
+            for (const Buf &x : mine)
+                for (const Buf &y : theirs) {
+                    const Buf pair[2] = {x, y};
+                    z3_status st = check_bufs(fn, pair, 2);
+                    if (st != Z3_OK) return st;
+                }
+            const Buf ug = {u.grads, u.layout->psi ? gu : 0, "a unit's grads"};
+            for (const Buf &y : their_w) {
+                const Buf pair[2] = {ug, y};
+                z3_status st = check_bufs(fn, pair, 2);
+                if (st != Z3_OK) return st;
+            }
+        }
+    }
     const cudaStream_t s = (cudaStream_t)stream;
     Range range("z3/model_step");
     z3_status st = Z3_OK;
+    // whether this call has enqueued a kernel on s (on g) yet: a launch may
+    // read early only after one of its own
+    bool ours_s = false, ours_g = false;
     // the update of unit i; a resident unit is gathered into its own copy
-    // right after it, on the same stream
+    // right after it, on the same stream (that gather reads the shards the
+    // update just wrote, so it never reads early)
     auto update = [&](int32_t i) -> z3_status {
         const z3_layout *L = units[i].layout;
         if (L->psi_padded == 0) return Z3_OK;
         z3_status us;
         {
             Range r("z3/ReduceScatter+Adam");
-            us = run_reduce(L, args[i], kRSAdam, s, fn);
+            us = run_reduce(L, args[i], kRSAdam, s, fn, ours_s);
+            ours_s = true;
         }
         if (us != Z3_OK || units[i].resident == nullptr || L->psi == 0) return us;
         Range r("z3/AllGather(resident)");
-        return run_allgather(L, units[i].shards, units[i].resident, s);
+        return run_allgather(L, units[i].shards, units[i].resident, s, false);
     };
     if (n_full == 1) {
         for (int32_t i = 0; i < n_units && st == Z3_OK; ++i) {
             Range r("z3/AllGather(forward)");
-            if (units[i].layout->psi && !units[i].resident)
-                st = run_allgather(units[i].layout, units[i].shards, full[0], s);
+            if (units[i].layout->psi && !units[i].resident) {
+                st = run_allgather(units[i].layout, units[i].shards, full[0], s, ours_s);
+                ours_s = true;
+            }
         }
         for (int32_t i = n_units - 1; i >= 0 && st == Z3_OK; --i) {
             const z3_layout *L = units[i].layout;
             if (L->psi && !units[i].resident) {
                 Range r("z3/AllGather(backward)");
-                st = run_allgather(L, units[i].shards, full[0], s);
+                st = run_allgather(L, units[i].shards, full[0], s, ours_s);
+                ours_s = true;
             }
             if (st == Z3_OK) st = update(i);
         }
@@ -436,8 +492,10 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
     if ((err = cudaStreamWaitEvent(g, E.ev[0], 0)) != cudaSuccess) return cuda_fail(err);
     for (int32_t i = 0; i < n_units && st == Z3_OK; ++i) {
         Range r("z3/AllGather(forward)");
-        if (units[i].layout->psi && !units[i].resident)
-            st = run_allgather(units[i].layout, units[i].shards, full[i % nb], g);
+        if (units[i].layout->psi && !units[i].resident) {
+            st = run_allgather(units[i].layout, units[i].shards, full[i % nb], g, ours_g);
+            ours_g = true;
+        }
     }
     std::vector<bool> buffer_used((size_t)nb, false);
     auto gather = [&](int32_t i) -> z3_status {
@@ -447,9 +505,11 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
             if (e != cudaSuccess) return cuda_fail(e);
         }
         Range r("z3/AllGather(backward)");
-        z3_status gs = units[i].layout->psi && !units[i].resident
-                           ? run_allgather(units[i].layout, units[i].shards, full[b], g)
-                           : Z3_OK;
+        z3_status gs = Z3_OK;
+        if (units[i].layout->psi && !units[i].resident) {
+            gs = run_allgather(units[i].layout, units[i].shards, full[b], g, ours_g);
+            ours_g = true;
+        }
         if (gs != Z3_OK) return gs;
         cudaError_t e = cudaEventRecord(gathered(b), g);
         return e == cudaSuccess ? Z3_OK : cuda_fail(e);

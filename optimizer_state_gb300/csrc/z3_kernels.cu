@@ -126,15 +126,23 @@ __device__ __forceinline__ TileRef locate(const Tab &tab, int64_t g) {
     return TileRef{lo, r, local - r * tpc};
 }
 
-// Programmatic dependent launch.  Every kernel lets the next kernel of the
-// stream launch at once (its CTAs then wait), and waits for the previous
-// kernel to complete -- memory included -- before its first global memory
-// access.  Ordering between the calls is therefore exactly stream order; only
-// the launch latency of a kernel overlaps the tail of the one before it.
+// Programmatic dependent launch.  Every kernel is launched so that it may
+// start while the previous kernel of the stream (its primary) still runs.
+// A thread first waits for the primary to complete -- memory included -- and
+// only then lets the next kernel launch.  Because every kernel waits before
+// it releases its dependent, a kernel that has started knows that everything
+// enqueued before its primary has completed: only the primary may still be
+// running.  So:
+//   - a plain kernel waits before its first global memory access, and the
+//     ordering between calls is exactly stream order;
+//   - an EARLY variant (used only where the library itself enqueued the
+//     primary, inside one call) may, before it waits, read buffers that the
+//     primary does not write; it waits before its first store.  Its first
+//     loads overlap the primary's tail.
 // Without the launch attribute both instructions are no-ops.
 __device__ __forceinline__ void pdl_enter() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // --------------------------------------------------------------------------
@@ -146,7 +154,7 @@ struct GatherArgs {
     uint16_t *__restrict__ full;
 };
 
-template <int PHI>
+template <int PHI, bool EARLY>
 __device__ __forceinline__ void gather_tile(const Tab &tab, const GatherArgs &a, int64_t d0,
                                             int64_t len, int64_t delta, int64_t qbeg,
                                             int64_t qend) {
@@ -169,6 +177,7 @@ __device__ __forceinline__ void gather_tile(const Tab &tab, const GatherArgs &a,
             }
         }
     }
+    if constexpr (EARLY) pdl_enter();  // the shard loads above may precede it; stores may not
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
         const int64_t q = qbeg + (int64_t)i * kGatherThreads + threadIdx.x;
@@ -184,10 +193,12 @@ __device__ __forceinline__ void gather_tile(const Tab &tab, const GatherArgs &a,
     }
 }
 
-template <bool ALIGNED>
+// EARLY: the primary writes neither the shards nor anything else read here
+// (it may write `full`: the stores wait).
+template <bool ALIGNED, bool EARLY>
 __global__ void __launch_bounds__(kGatherThreads)
 k_allgather(const __grid_constant__ Tab tab, const GatherArgs a) {
-    pdl_enter();
+    if constexpr (!EARLY) pdl_enter();
     const TileRef tr = locate(tab, blockIdx.x);
     const TabEntry &e = tab.e[tr.p];
     const int64_t d0 = e.F + tr.r * e.s;
@@ -200,18 +211,18 @@ k_allgather(const __grid_constant__ Tab tab, const GatherArgs a) {
     const int64_t qend = min(q_last + 1, qbeg + (int64_t)(kGatherThreads * kGatherVecPerThread));
     const int64_t delta = d0 - (tr.r * tab.S + e.o);
     if constexpr (ALIGNED) {
-        gather_tile<0>(tab, a, d0, len, delta, qbeg, qend);
+        gather_tile<0, EARLY>(tab, a, d0, len, delta, qbeg, qend);
     } else {
         const int phi = (int)((((-delta) % kVec) + kVec) % kVec);
         switch (phi) {
-            case 0: gather_tile<0>(tab, a, d0, len, delta, qbeg, qend); break;
-            case 1: gather_tile<1>(tab, a, d0, len, delta, qbeg, qend); break;
-            case 2: gather_tile<2>(tab, a, d0, len, delta, qbeg, qend); break;
-            case 3: gather_tile<3>(tab, a, d0, len, delta, qbeg, qend); break;
-            case 4: gather_tile<4>(tab, a, d0, len, delta, qbeg, qend); break;
-            case 5: gather_tile<5>(tab, a, d0, len, delta, qbeg, qend); break;
-            case 6: gather_tile<6>(tab, a, d0, len, delta, qbeg, qend); break;
-            default: gather_tile<7>(tab, a, d0, len, delta, qbeg, qend); break;
+            case 0: gather_tile<0, EARLY>(tab, a, d0, len, delta, qbeg, qend); break;
+            case 1: gather_tile<1, EARLY>(tab, a, d0, len, delta, qbeg, qend); break;
+            case 2: gather_tile<2, EARLY>(tab, a, d0, len, delta, qbeg, qend); break;
+            case 3: gather_tile<3, EARLY>(tab, a, d0, len, delta, qbeg, qend); break;
+            case 4: gather_tile<4, EARLY>(tab, a, d0, len, delta, qbeg, qend); break;
+            case 5: gather_tile<5, EARLY>(tab, a, d0, len, delta, qbeg, qend); break;
+            case 6: gather_tile<6, EARLY>(tab, a, d0, len, delta, qbeg, qend); break;
+            default: gather_tile<7, EARLY>(tab, a, d0, len, delta, qbeg, qend); break;
         }
     }
 }
@@ -255,7 +266,7 @@ __device__ __forceinline__ void finish1(const ReduceArgs &a, int64_t x, float g,
     }
 }
 
-template <int PHI, int MODE>
+template <int PHI, int MODE, bool EARLY>
 __device__ __forceinline__ void reduce_vector(const ReduceArgs &a, int n_ranks, int64_t x0,
                                               int64_t delta) {
     // Rank fold first (8 ranks' 16-byte loads in flight per batch), then the
@@ -314,6 +325,7 @@ __device__ __forceinline__ void reduce_vector(const ReduceArgs &a, int n_ranks, 
         }
 #pragma unroll
         for (int l = 0; l < 8; ++l) adam1(g[l], p[l], m[l], v[l], a.k);
+        if constexpr (EARLY) pdl_enter();  // every load above may precede it; stores may not
         st8f(a.master + x0, p);
         st8f(a.m + x0, m);
         st8f(a.v + x0, v);
@@ -329,7 +341,7 @@ __device__ __forceinline__ void reduce_vector(const ReduceArgs &a, int n_ranks, 
 // --------------------------------------------------------------------------
 // Reduce for tables whose chunks all have phase 0 (every transformer layout
 // whose parameter sizes divide by 8N).  One vector per thread; the kernel is
-// kept at <= 64 registers so that four 256-thread CTAs (32 warps) share an
+// kept at <= 64 registers so that eight 128-thread CTAs (32 warps) share an
 // SM: with eight 16-byte gradient loads and six 16-byte state loads in
 // flight per thread, that is enough memory-level parallelism to hide HBM
 // latency while the Adam arithmetic of other warps runs.
@@ -358,11 +370,15 @@ __device__ __noinline__ void reduce_edges(const ReduceArgs a, int n_ranks, int64
     }
 }
 
-template <int MODE>
+// EARLY (fused modes only): the primary writes none of the buffers read here
+// (gradients, running sums, master, m, v); it may read or write others, and
+// every store waits for it.
+template <int MODE, bool EARLY>
 __global__ void __launch_bounds__(kReduceThreads, 1024 / kReduceThreads)
 k_reduce_aligned(const __grid_constant__ Tab tab, const ReduceArgs a) {
     static_assert(kReduceVecPerThread == 1, "one vector per thread");
-    pdl_enter();
+    static_assert(!EARLY || MODE == kRSAdam || MODE == kRSAccAdam, "EARLY: fused modes only");
+    if constexpr (!EARLY) pdl_enter();
     const TileRef tr = locate(tab, blockIdx.x);
     const TabEntry &e = tab.e[tr.p];
     const int64_t c0 = tr.r * tab.S + e.o;
@@ -371,18 +387,21 @@ k_reduce_aligned(const __grid_constant__ Tab tab, const ReduceArgs a) {
     const int64_t delta = e.F + tr.r * e.s - c0;
     const int64_t x0 = (c0 / kVec + tr.t * (int64_t)kReduceThreads + threadIdx.x) * kVec;
     if (x0 >= c_end) return;  // past the chunk's last vector
-    if (x0 >= c0 && x0 + kVec <= valid_end)
-        reduce_vector<0, MODE>(a, tab.n_ranks, x0, delta);
-    else
+    if (x0 >= c0 && x0 + kVec <= valid_end) {
+        reduce_vector<0, MODE, EARLY>(a, tab.n_ranks, x0, delta);
+    } else {
+        if constexpr (EARLY) pdl_enter();
         reduce_edges<MODE>(a, tab.n_ranks, x0, delta, c0, c_end, valid_end);
+    }
 }
 
 // The same for tables whose chunks have other phases: each chunk's phase
 // (uniform per CTA) selects a window-shifting instantiation.
-template <int MODE>
+template <int MODE, bool EARLY>
 __global__ void __launch_bounds__(kReduceThreads, 1024 / kReduceThreads)
 k_reduce_shifted(const __grid_constant__ Tab tab, const ReduceArgs a) {
-    pdl_enter();
+    static_assert(!EARLY || MODE == kRSAdam || MODE == kRSAccAdam, "EARLY: fused modes only");
+    if constexpr (!EARLY) pdl_enter();
     const TileRef tr = locate(tab, blockIdx.x);
     const TabEntry &e = tab.e[tr.p];
     const int64_t c0 = tr.r * tab.S + e.o;
@@ -392,19 +411,20 @@ k_reduce_shifted(const __grid_constant__ Tab tab, const ReduceArgs a) {
     const int64_t x0 = (c0 / kVec + tr.t * (int64_t)kReduceThreads + threadIdx.x) * kVec;
     if (x0 >= c_end) return;
     if (!(x0 >= c0 && x0 + kVec <= valid_end)) {
+        if constexpr (EARLY) pdl_enter();
         reduce_edges<MODE>(a, tab.n_ranks, x0, delta, c0, c_end, valid_end);
         return;
     }
     const int n = tab.n_ranks;
     switch ((int)(((delta % kVec) + kVec) % kVec)) {
-        case 0: reduce_vector<0, MODE>(a, n, x0, delta); break;
-        case 1: reduce_vector<1, MODE>(a, n, x0, delta); break;
-        case 2: reduce_vector<2, MODE>(a, n, x0, delta); break;
-        case 3: reduce_vector<3, MODE>(a, n, x0, delta); break;
-        case 4: reduce_vector<4, MODE>(a, n, x0, delta); break;
-        case 5: reduce_vector<5, MODE>(a, n, x0, delta); break;
-        case 6: reduce_vector<6, MODE>(a, n, x0, delta); break;
-        default: reduce_vector<7, MODE>(a, n, x0, delta); break;
+        case 0: reduce_vector<0, MODE, EARLY>(a, n, x0, delta); break;
+        case 1: reduce_vector<1, MODE, EARLY>(a, n, x0, delta); break;
+        case 2: reduce_vector<2, MODE, EARLY>(a, n, x0, delta); break;
+        case 3: reduce_vector<3, MODE, EARLY>(a, n, x0, delta); break;
+        case 4: reduce_vector<4, MODE, EARLY>(a, n, x0, delta); break;
+        case 5: reduce_vector<5, MODE, EARLY>(a, n, x0, delta); break;
+        case 6: reduce_vector<6, MODE, EARLY>(a, n, x0, delta); break;
+        default: reduce_vector<7, MODE, EARLY>(a, n, x0, delta); break;
     }
 }
 
@@ -635,12 +655,12 @@ void launch(void (*kernel)(KArgs...), int64_t grid, int block, cudaStream_t stre
     (void)cudaLaunchKernelEx(&cfg, kernel, args...);  // errors: cudaGetLastError below
 }
 
-template <int MODE>
+template <int MODE, bool EARLY>
 void launch_reduce_tab(const Tab &t, const ReduceArgs &a, cudaStream_t stream) {
     if (t.phase0)
-        launch(k_reduce_aligned<MODE>, t.tiles, kReduceThreads, stream, t, a);
+        launch(k_reduce_aligned<MODE, EARLY>, t.tiles, kReduceThreads, stream, t, a);
     else
-        launch(k_reduce_shifted<MODE>, t.tiles, kReduceThreads, stream, t, a);
+        launch(k_reduce_shifted<MODE, EARLY>, t.tiles, kReduceThreads, stream, t, a);
 }
 
 }  // namespace
@@ -655,25 +675,45 @@ cudaError_t launch_partition(const z3_layout *L, const PartitionArgs &a, cudaStr
 }
 
 cudaError_t launch_allgather(const z3_layout *L, const uint16_t *shards, uint16_t *full,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, bool early) {
     const GatherArgs a{shards, full};
+    bool first = true;
     for (const Tab &t : L->gather_tabs) {
-        if (t.phase0)
-            launch(k_allgather<true>, t.tiles, kGatherThreads, stream, t, a);
-        else
-            launch(k_allgather<false>, t.tiles, kGatherThreads, stream, t, a);
+        // a later table's primary is this call's own previous launch, which
+        // writes only `full`
+        const bool e = early || !first;
+        first = false;
+        if (t.phase0) {
+            if (e) launch(k_allgather<true, true>, t.tiles, kGatherThreads, stream, t, a);
+            else launch(k_allgather<true, false>, t.tiles, kGatherThreads, stream, t, a);
+        } else {
+            if (e) launch(k_allgather<false, true>, t.tiles, kGatherThreads, stream, t, a);
+            else launch(k_allgather<false, false>, t.tiles, kGatherThreads, stream, t, a);
+        }
     }
     return cudaGetLastError();
 }
 
 cudaError_t launch_reduce(const z3_layout *L, const ReduceArgs &a, Mode mode,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool early) {
+    // Later tables of one call update disjoint shard ranges, so their
+    // primary (this call's previous table) writes nothing they read; an
+    // unfused mode reads its own output buffer, so it never runs early.
+    bool first = true;
     for (const Tab &t : L->reduce_tabs) {
+        const bool e = early || !first;
+        first = false;
         switch (mode) {
-            case kRS: launch_reduce_tab<kRS>(t, a, stream); break;
-            case kRSAcc: launch_reduce_tab<kRSAcc>(t, a, stream); break;
-            case kRSAdam: launch_reduce_tab<kRSAdam>(t, a, stream); break;
-            default: launch_reduce_tab<kRSAccAdam>(t, a, stream); break;
+            case kRS: launch_reduce_tab<kRS, false>(t, a, stream); break;
+            case kRSAcc: launch_reduce_tab<kRSAcc, false>(t, a, stream); break;
+            case kRSAdam:
+                if (e) launch_reduce_tab<kRSAdam, true>(t, a, stream);
+                else launch_reduce_tab<kRSAdam, false>(t, a, stream);
+                break;
+            default:
+                if (e) launch_reduce_tab<kRSAccAdam, true>(t, a, stream);
+                else launch_reduce_tab<kRSAccAdam, false>(t, a, stream);
+                break;
         }
     }
     return cudaGetLastError();

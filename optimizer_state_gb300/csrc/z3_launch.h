@@ -83,10 +83,15 @@ inline int64_t flat_blocks(int64_t total, int threads) {
 }
 
 cudaError_t launch_partition(const z3_layout *L, const PartitionArgs &a, cudaStream_t stream);
+// early: the kernel of this stream just before this launch was enqueued by
+// the library in the same call and writes nothing this launch reads (for
+// the gather: not the shards; for a fused reduce: not the gradients, running
+// sums, master, m or v).  The launch may then read before it waits for that
+// kernel (its stores still wait).  Ignored by the unfused reduce modes.
 cudaError_t launch_allgather(const z3_layout *L, const uint16_t *shards, uint16_t *full,
-                             cudaStream_t stream);
+                             cudaStream_t stream, bool early);
 cudaError_t launch_reduce(const z3_layout *L, const ReduceArgs &a, Mode mode,
-                          cudaStream_t stream);
+                          cudaStream_t stream, bool early);
 cudaError_t launch_adam(const AdamArgs &a, cudaStream_t stream);
 cudaError_t launch_allreduce(const AllreduceArgs &a, cudaStream_t stream);
 cudaError_t launch_scatter(const z3_layout *L, const ScatterArgs &a, cudaStream_t stream);

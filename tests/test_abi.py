@@ -202,6 +202,10 @@ def test_model_step_validation_without_gpu(lib):
     assert s == z3.Z3_ERR_ALIGNMENT and "resident" in msg
     s, msg = call([unit(A), unit(A + (8 << 20), resident=full + 16)], [full])
     assert s == z3.Z3_ERR_INVALID_ARG and "overlaps" in msg      # resident inside full
+    s, msg = call([unit(A), unit(A + (2 << 20))], [full])        # two units share state
+    assert s == z3.Z3_ERR_INVALID_ARG and "another unit" in msg
+    s, msg = call([unit(A), unit(A + (8 << 20), resident=A + (4 << 20))], [full])
+    assert s == z3.Z3_ERR_INVALID_ARG and "another unit" in msg  # resident over another's grads
     assert T == 64
 
 
