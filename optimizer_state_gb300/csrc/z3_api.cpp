@@ -360,6 +360,7 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
         if (units[i].resident == nullptr) full_bytes = std::max(full_bytes, 2 * units[i].layout->psi);
     }
     std::vector<ReduceArgs> args((size_t)n_units);
+    std::vector<int64_t> grad_bytes((size_t)n_units, 0);
     for (int32_t i = 0; i < n_units; ++i) {
         const z3_unit &u = units[i];
         z3_status st = prepare_rs_adam(fn, u.layout, u.grads, u.grad_stride, u.scale, nullptr,
@@ -370,6 +371,7 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
         int64_t gbytes = 0;
         st = check_grads(fn, u.layout, u.grad_stride, &gbytes);
         if (st != Z3_OK) return st;
+        grad_bytes[(size_t)i] = u.layout->psi ? gbytes : 0;
         for (int32_t k = 0; k < n_full; ++k) {
             const Buf bufs[7] = {{full[k], full_bytes, "full[k]"},
                                  {u.resident, u.resident ? 2 * u.layout->psi : 0, "resident"},
@@ -399,9 +401,6 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
         for (int32_t j = i + 1; j < n_units; ++j) {
             const z3_unit &w = units[j];
             const int64_t Tw = w.layout->psi_padded;
-            int64_t gu = 0, gw = 0;
-            check_grads(fn, u.layout, u.grad_stride, &gu);
-            check_grads(fn, w.layout, w.grad_stride, &gw);
             const Buf mine[5] = {{u.shards, 2 * T, "a unit's shards"},
                                  {u.master, 4 * T, "a unit's master"},
                                  {u.m, 4 * T, "a unit's m"},
@@ -414,7 +413,7 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
                                    {w.v, 4 * Tw, "another unit's v"},
                                    {w.resident, w.resident ? 2 * w.layout->psi : 0,
                                     "another unit's resident copy"},
-                                   {w.grads, w.layout->psi ? gw : 0, "another unit's grads"}};
+                                   {w.grads, grad_bytes[(size_t)j], "another unit's grads"}};
             const Buf their_w[5] = {theirs[0], theirs[1], theirs[2], theirs[3], theirs[4]};
             for (const Buf &x : mine)
                 for (const Buf &y : theirs) {
@@ -422,7 +421,7 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
                     z3_status st = check_bufs(fn, pair, 2);
                     if (st != Z3_OK) return st;
                 }
-            const Buf ug = {u.grads, u.layout->psi ? gu : 0, "a unit's grads"};
+            const Buf ug = {u.grads, grad_bytes[(size_t)i], "a unit's grads"};
             for (const Buf &y : their_w) {
                 const Buf pair[2] = {ug, y};
                 z3_status st = check_bufs(fn, pair, 2);
