@@ -322,3 +322,53 @@ def test_model_step_matches_oracle(z3mod, orc, depth):
         for b, fb in last_bwd.items():
             assert np.array_equal(u16(fulls[b].t)[:fb.size], fb), f"buffer {b}"
         assert all(f.guards_intact() for f in fulls)
+
+
+def _fuzz_model_configs(n=12, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        N = int(rng.choice([1, 2, 3, 5, 8, 16]))
+        units = []
+        for _ in range(int(rng.integers(1, 7))):
+            numel = [int(x) for x in rng.integers(0, 20000, size=int(rng.integers(1, 9)))]
+            if rng.random() < 0.2:
+                numel[0] = 0
+            units.append((numel, bool(rng.random() < 0.25)))
+        out.append((N, units, int(rng.integers(0, 4))))
+    return out
+
+
+@pytest.mark.parametrize("N,specs,depth", _fuzz_model_configs())
+def test_model_step_fuzzed(z3mod, orc, N, specs, depth):
+    """Seeded random models through z3_model_step: 1-6 units of 1-8
+    parameters (empty ones included), some resident, N_d from 1 to 16,
+    prefetch depth 0-3; two steps against the oracle's layer step, bit for
+    bit, with guard words around every buffer."""
+    if all(res for _, res in specs):
+        specs = [(specs[0][0], False)] + list(specs[1:])
+    cases = [Case(z3mod, orc, numel, N, seed=300 + i) for i, (numel, _) in enumerate(specs)]
+    resident = [Guarded(max(c.L.psi, 1), torch.bfloat16) if res else None
+                for c, (_, res) in zip(cases, specs)]
+    for c, r in zip(cases, resident):
+        if r is not None:
+            z3mod.z3_allgather(c.L, c.shards.t, r.t)
+    big = max([c.L.psi for c, (_, res) in zip(cases, specs) if not res] + [1])
+    fulls = [Guarded(big, torch.bfloat16) for _ in range(depth + 1)]
+    gstream = torch.cuda.Stream() if depth else None
+    for t in (1, 2):
+        drawn = [c.grads() for c in cases]
+        units = [(c.L, c.shards.t, c.master.t, c.m.t, c.v.t, g, c.stride, 1.0 / N,
+                  None if r is None else r.t) for c, (g, _), r in zip(cases, drawn, resident)]
+        z3mod.z3_model_step(units, [f.t for f in fulls], HP, t, gather_stream=gstream)
+        for c, (_, gh) in zip(cases, drawn):
+            orc.step_layer(c.O, c.o["shards"], gh, c.stride, 1.0 / N, c.o["master"], c.o["m"],
+                           c.o["v"], HP, t)
+        torch.cuda.synchronize()
+        for c, r in zip(cases, resident):
+            assert_adam_equal(c.device_state(), c.o)
+            assert c.guards_ok()
+            if r is not None:
+                assert np.array_equal(u16(r.t)[:c.L.psi], orc.allgather(c.O, c.o["shards"]))
+                assert r.guards_intact()
+        assert all(f.guards_intact() for f in fulls)
