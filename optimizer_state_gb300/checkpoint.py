@@ -14,7 +14,9 @@ Format (directory):
 ``save`` synchronises the device before copying (the caller must be between
 steps).  ``load`` verifies every rank file is present and intact -- a missing
 file is a lost rank, reported by number -- and reshards on the device when the
-requested rank count differs from the saved one.
+requested rank count differs from the saved one.  ``save_model`` /
+``load_model`` do the same for every unit of a multi-unit model, one shard set
+per unit, and rebuild resident copies from the loaded shards.
 """
 from __future__ import annotations
 
@@ -134,3 +136,54 @@ def load(path: str, n_ranks: int | None = None, device="cuda"):
         out[name] = o
     torch.cuda.synchronize()
     return dst, out, meta["step"]
+
+
+MODEL_FORMAT = "z3-model-v1"
+
+
+def save_model(path: str, model):
+    """Save every unit of a multi-unit model (``schedule.Model``) between
+    steps: one per-rank shard set per unit under ``unit%03d/`` and a
+    ``model.json`` with the units' names, parameter counts, resident flags and
+    the step counter.  A resident unit's gathered copy is not saved: it is a
+    function of the shards."""
+    os.makedirs(path, exist_ok=True)
+    units = []
+    for i, u in enumerate(model.units):
+        sub = f"unit{i:03d}"
+        save(os.path.join(path, sub), u.L, u.shards, u.master, u.m, u.v, model.t)
+        units.append({"dir": sub, "name": u.w.name, "numel": [int(n) for n in u.L.numel],
+                      "resident": u.resident is not None})
+    with open(os.path.join(path, "model.json"), "w") as f:
+        json.dump({"format": MODEL_FORMAT, "step": int(model.t), "units": units}, f, indent=1)
+
+
+def load_model(path: str, model):
+    """Load a saved model into ``model``, whose units must hold the same
+    parameters in the same order (each unit may use another rank count: its
+    state is resharded on the device).  Resident copies are gathered again
+    from the loaded shards, and the model's step counter is restored."""
+    import torch
+
+    from . import z3
+    try:
+        with open(os.path.join(path, "model.json")) as f:
+            meta = json.load(f)
+    except OSError as e:
+        raise CheckpointError(f"no model metadata in {path}: {e}") from e
+    if meta.get("format") != MODEL_FORMAT:
+        raise CheckpointError(f"unknown model checkpoint format {meta.get('format')!r}")
+    if len(meta["units"]) != len(model.units):
+        raise CheckpointError(f"checkpoint has {len(meta['units'])} units, the model "
+                              f"{len(model.units)}")
+    for i, (m, u) in enumerate(zip(meta["units"], model.units)):
+        if m["numel"] != [int(n) for n in u.L.numel]:
+            raise CheckpointError(f"unit {i}: the saved parameters differ from the model's")
+        L, tensors, _ = load(os.path.join(path, m["dir"]), n_ranks=u.L.n_ranks,
+                             device=u.shards.device)
+        for name in ("shards", "master", "m", "v"):
+            getattr(u, name).copy_(tensors[name])
+        if u.resident is not None:
+            z3.z3_allgather(u.L, u.shards, u.resident)
+    model.t = int(meta["step"])
+    torch.cuda.synchronize()

@@ -50,3 +50,27 @@ def test_corruption_and_truncation_detected(orc, tmp_path):
         ck.read_host(str(tmp_path))
     with pytest.raises(ck.CheckpointError, match="metadata"):
         ck.read_host(str(tmp_path / "nowhere"))
+
+
+def test_model_metadata_checks(tmp_path):
+    """load_model refuses a missing or foreign model file, another unit count
+    and other parameters before it touches any device buffer."""
+    import json
+    from types import SimpleNamespace as NS
+
+    def fake_model(numels):
+        return NS(units=[NS(L=NS(numel=n, n_ranks=4)) for n in numels], t=0)
+    d = tmp_path / "m"
+    with pytest.raises(ck.CheckpointError, match="no model metadata"):
+        ck.load_model(str(d), fake_model([[5, 3]]))
+    d.mkdir()
+    (d / "model.json").write_text(json.dumps({"format": "other", "units": []}))
+    with pytest.raises(ck.CheckpointError, match="unknown model checkpoint format"):
+        ck.load_model(str(d), fake_model([[5, 3]]))
+    units = [{"dir": "unit000", "name": "a", "numel": [5, 3], "resident": False}]
+    (d / "model.json").write_text(json.dumps({"format": ck.MODEL_FORMAT, "step": 3,
+                                              "units": units}))
+    with pytest.raises(ck.CheckpointError, match="units"):
+        ck.load_model(str(d), fake_model([[5, 3], [7]]))
+    with pytest.raises(ck.CheckpointError, match="parameters differ"):
+        ck.load_model(str(d), fake_model([[5, 4]]))

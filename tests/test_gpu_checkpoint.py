@@ -113,3 +113,63 @@ def test_save_load_resume(mods, orc, tmp_path):
         torch.cuda.synchronize()
         assert np.array_equal(bits32(f32(s2["master"])), bits32(ma))
         assert np.array_equal(u16(s2["shards"]), sh)
+
+
+def _model(sch, dev, seed, n_ranks, depth):
+    """A small three-unit model: a resident unit of small parameters and two
+    layers of odd lengths, every unit at n_ranks."""
+    ws = [I.Workload("res", ((77,), (1024,)), n_ranks, 0.02, 1e-3, resident=True),
+          I.Workload("l0", ((100003,), (4099,), (3, 7)), n_ranks, 0.02, 1e-3),
+          I.Workload("l1", ((65536,), (262147,)), n_ranks, 0.02, 1e-3)]
+    gen = I.make_generator(seed, dev)
+    units = [sch.Unit(w, dev, gen) for w in ws]
+    return sch.PrefetchModel(units, dev, depth) if depth else sch.Model(units, dev)
+
+
+@pytest.mark.parametrize("n_src,n_dst,depth", [(4, 4, 0), (4, 4, 2), (6, 3, 1)])
+def test_model_save_load_resume(mods, tmp_path, n_src, n_dst, depth):
+    """A whole model (resident unit included) saved between steps and loaded
+    into another model: every unit's gathered parameters and fp32 state equal
+    the saved model's (resharded on the device when the rank count differs),
+    the resident copy is rebuilt from the loaded shards and the step counter
+    is restored.  At the same rank count, two more steps on both models agree
+    bit for bit."""
+    z3, sch, ckpt = mods
+    dev = torch.device("cuda")
+    a = _model(sch, dev, 11, n_src, depth)
+    for _ in range(2):
+        a.step(HP)
+    ckpt.save_model(str(tmp_path / "m"), a)
+    b = _model(sch, dev, 99, n_dst, depth)          # another initial state, then loaded
+    if n_src == n_dst:
+        for ub, ua in zip(b.units, a.units):        # the same gradients from here on
+            ub.grads.copy_(ua.grads)
+    ckpt.load_model(str(tmp_path / "m"), b)
+    assert b.t == a.t == 2
+
+    def per_unit(model, name):
+        out = []
+        for u in model.units:
+            L1 = z3.Layout(u.w.numel, 1)
+            dt = torch.bfloat16 if name == "shards" else torch.float32
+            t = torch.empty(u.L.psi, dtype=dt, device=dev)
+            z3.z3_reshard(u.L, L1, getattr(u, name), t)
+            out.append(t)
+        return out
+    for name in ("shards", "master", "m", "v"):
+        for x, y in zip(per_unit(a, name), per_unit(b, name)):
+            vt = torch.int16 if name == "shards" else torch.int32
+            assert torch.equal(x.view(vt), y.view(vt)), name
+    assert torch.equal(a.units[0].resident.view(torch.int16), b.units[0].resident.view(torch.int16))
+    if n_src == n_dst:
+        for _ in range(2):
+            a.step(HP)
+            b.step(HP)
+        torch.cuda.synchronize()
+        for ua, ub in zip(a.units, b.units):
+            for name in ("master", "m", "v"):
+                assert torch.equal(getattr(ua, name).view(torch.int32),
+                                   getattr(ub, name).view(torch.int32)), name
+            assert torch.equal(ua.shards.view(torch.int16), ub.shards.view(torch.int16))
+        assert torch.equal(a.units[0].resident.view(torch.int16),
+                           b.units[0].resident.view(torch.int16))
