@@ -394,39 +394,50 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
     // other unit: a launch then never reads what its stream predecessor (a
     // launch of another unit, or of this unit's gather) writes, which lets
     // the gathers read shards and the updates read gradients and state
-    // before they wait for that predecessor.
-    for (int32_t i = 0; i < n_units; ++i) {
-        const z3_unit &u = units[i];
-        const int64_t T = u.layout->psi_padded;
-        for (int32_t j = i + 1; j < n_units; ++j) {
-            const z3_unit &w = units[j];
-            const int64_t Tw = w.layout->psi_padded;
-            const Buf mine[5] = {{u.shards, 2 * T, "a unit's shards"},
-                                 {u.master, 4 * T, "a unit's master"},
-                                 {u.m, 4 * T, "a unit's m"},
-                                 {u.v, 4 * T, "a unit's v"},
-                                 {u.resident, u.resident ? 2 * u.layout->psi : 0,
-                                  "a unit's resident copy"}};
-            const Buf theirs[6] = {{w.shards, 2 * Tw, "another unit's shards"},
-                                   {w.master, 4 * Tw, "another unit's master"},
-                                   {w.m, 4 * Tw, "another unit's m"},
-                                   {w.v, 4 * Tw, "another unit's v"},
-                                   {w.resident, w.resident ? 2 * w.layout->psi : 0,
-                                    "another unit's resident copy"},
-                                   {w.grads, grad_bytes[(size_t)j], "another unit's grads"}};
-            const Buf their_w[5] = {theirs[0], theirs[1], theirs[2], theirs[3], theirs[4]};
-            for (const Buf &x : mine)
-                for (const Buf &y : theirs) {
-                    const Buf pair[2] = {x, y};
-                    z3_status st = check_bufs(fn, pair, 2);
-                    if (st != Z3_OK) return st;
-                }
-            const Buf ug = {u.grads, grad_bytes[(size_t)i], "a unit's grads"};
-            for (const Buf &y : their_w) {
-                const Buf pair[2] = {ug, y};
-                z3_status st = check_bufs(fn, pair, 2);
-                if (st != Z3_OK) return st;
+    // before they wait for that predecessor.  Units may share read-only
+    // gradients.  A sweep over the buffers sorted by address finds every
+    // overlap in O(B log B) for B buffers (plus the overlaps themselves).
+    {
+        struct Span {
+            uintptr_t lo, hi;
+            int32_t unit;
+            bool written;
+            const char *name;
+        };
+        std::vector<Span> spans;
+        spans.reserve((size_t)n_units * 6);
+        auto add = [&](const void *p, int64_t bytes, int32_t unit, bool written,
+                       const char *name) {
+            if (bytes <= 0) return;
+            const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+            spans.push_back({lo, lo + (uintptr_t)bytes, unit, written, name});
+        };
+        for (int32_t i = 0; i < n_units; ++i) {
+            const z3_unit &u = units[i];
+            const int64_t T = u.layout->psi_padded;
+            add(u.shards, 2 * T, i, true, "shards");
+            add(u.master, 4 * T, i, true, "master");
+            add(u.m, 4 * T, i, true, "m");
+            add(u.v, 4 * T, i, true, "v");
+            add(u.resident, u.resident ? 2 * u.layout->psi : 0, i, true, "resident copy");
+            add(u.grads, grad_bytes[(size_t)i], i, false, "grads");
+        }
+        std::sort(spans.begin(), spans.end(),
+                  [](const Span &a, const Span &b) { return a.lo < b.lo; });
+        std::vector<const Span *> open;   // spans that may still overlap the next one
+        for (const Span &x : spans) {
+            size_t keep = 0;
+            for (const Span *y : open) {
+                if (y->hi <= x.lo) continue;  // ended before x starts
+                open[keep++] = y;
+                if (y->unit != x.unit && (y->written || x.written))
+                    return fail(Z3_ERR_INVALID_ARG,
+                                std::string(fn) + ": unit " + std::to_string(y->unit) + "'s " +
+                                    y->name + " overlaps another unit's (" +
+                                    std::to_string(x.unit) + ") " + x.name);
             }
+            open.resize(keep);
+            open.push_back(&x);
         }
     }
     const cudaStream_t s = (cudaStream_t)stream;

@@ -244,3 +244,28 @@ def test_host_step_validation_without_gpu(lib):
     assert lib.z3_host_step_run(None, A, A, A, 0.25, A, A, A, None, 1, None, None) == \
         z3.Z3_ERR_INVALID_ARG
     lib.z3_host_step_destroy(None)                           # a no-op
+
+
+def test_model_step_checks_many_units_quickly(lib):
+    """The cross-unit overlap check scales to thousands of units: 4000
+    disjoint units plus one whose master overlaps the first unit's shards
+    are rejected (naming both units) well within a second, before any CUDA
+    call."""
+    import time
+    L = z3.Layout([35, 13, 12], 4)
+    hp = z3.AdamHP(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    base = 1 << 36
+    n = 4000
+
+    def unit(a, master=None):
+        return z3.Unit(L.handle.value, a, master if master is not None else a + 1024, a + 2048,
+                       a + 3072, a + 4096, 64, 0.25, None)
+    units = [unit(base + i * 8192) for i in range(n)] + [unit(base + n * 8192, master=base + 64)]
+    arr = (z3.Unit * len(units))(*units)
+    full = (ctypes.c_void_p * 1)(base - (1 << 20))
+    t0 = time.perf_counter()
+    s = lib.z3_model_step(arr, len(units), full, 1, ctypes.byref(hp), 1, None, None)
+    dt = time.perf_counter() - t0
+    msg = z3.last_error()
+    assert s == z3.Z3_ERR_INVALID_ARG and "unit 0" in msg and f"({n})" in msg, msg
+    assert dt < 1.0, dt
