@@ -223,6 +223,24 @@ def run_cuda(args, world, rank, local):
         step(reps[i % n_rep])
     torch.cuda.synchronize()
 
+    graph = None
+    if args.graph:
+        # the K timed steps (each with its own step counter) captured once as
+        # one CUDA graph and replayed inside the timed region
+        if launches_per_step * args.steps > 50000:
+            raise SystemExit("--graph: too many launches in one graph; use fewer --steps")
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap), torch.cuda.graph(graph, stream=cap):
+            for i in range(args.steps):
+                rep = reps[i % n_rep]
+                rep.step += 1
+                z3.z3_step_layer(L, rep.shards, rep.full, rep.grads, w.grad_stride, scale,
+                                 rep.master, rep.m, rep.v, HP, rep.step, stream=cap.cuda_stream)
+        stream.wait_stream(cap)
+        torch.cuda.synchronize()
+
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -234,8 +252,11 @@ def run_cuda(args, world, rank, local):
     e1 = torch.cuda.Event(enable_timing=True)
     clocks.mark(True)
     e0.record(stream)
-    for i in range(args.steps):
-        step(reps[i % n_rep])
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(args.steps):
+            step(reps[i % n_rep])
     e1.record(stream)
     torch.cuda.synchronize()
     clocks.mark(False)
@@ -298,6 +319,8 @@ def run_cuda(args, world, rank, local):
                 "l2": f"{n_rep} rotating replicas of the layer state "
                       f"({n_rep * state_bytes / 1e9:.2f} GB > 129 MB L2), every step cold",
                 "parallelism": f"{world} independent replica(s), one per GPU",
+                "launch": (f"one CUDA graph of the {args.steps} timed steps" if args.graph
+                           else "stream launches"),
             },
             "params_per_s": round(world * L.psi * args.steps / (ms_max * 1e-3), 1),
             "pct_of_8tbs": round(100.0 * value / (NOMINAL_HBM_GBS * world), 2),
