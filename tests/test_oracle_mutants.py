@@ -36,6 +36,12 @@ MUTANTS = {
     "gathered slice reversed": (
         "src + (size_t)(r * S + shard_off[p] + j) * elem, elem);",
         "src + (size_t)(r * S + shard_off[p] + (shard_numel[p] - 1 - j)) * elem, elem);"),
+    "scale applied to each rank before the sum": (
+        FOLD + "\n    return acc * scale;",
+        """    float acc = or_f32_from_bf16(grads[e]) * scale;
+    for (int32_t k = 1; k < n_ranks; ++k)
+        acc = acc + or_f32_from_bf16(grads[(int64_t)k * grad_stride + e]) * scale;
+    return acc;"""),
     "accumulate drops the running sum": (
         "out[at] = accumulate ? out[at] + g : g;", "out[at] = g;"),
     "eps inside the square root": (
