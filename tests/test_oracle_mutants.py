@@ -51,6 +51,16 @@ MUTANTS = {
     "second-moment correction uses beta1": (
         "k.rb2 = (float)(1.0 / (1.0 - pow(beta2, (double)step)));",
         "k.rb2 = (float)(1.0 / (1.0 - pow(beta1, (double)step)));"),
+    "reduce-scatter leaves the pad untouched": (
+        """                if (i >= numel[p]) {
+                    out[at] = 0.0f;
+                    continue;
+                }""",
+        """                if (i >= numel[p]) {
+                    continue;
+                }"""),
+    "reduce-scatter reads the next rank's slice": (
+        "full_off[p] + i, scale);", "full_off[p] + (i + shard_numel[p] < numel[p] ? i + shard_numel[p] : i), scale);"),
     "accumulate drops the running sum": (
         "out[at] = accumulate ? out[at] + g : g;", "out[at] = g;"),
     "eps inside the square root": (
