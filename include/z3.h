@@ -236,9 +236,12 @@ typedef struct z3_unit {
  *     prefetch depth trades memory -- one more buffer per unit of depth --
  *     against latency).  Unit i uses full[i mod n_full]; events order every
  *     buffer reuse.  The call returns with `stream` ordered after all work.
- * Results do not depend on n_full.  Errors: as z3_step_layer for each unit,
- * n_units < 1, n_full not in 1..8, gather_stream NULL or equal to stream
- * when n_full >= 2, overlapping buffers. */
+ * Results do not depend on n_full.  Every buffer a unit writes (shards,
+ * master, m, v, resident) must be disjoint from every buffer of every other
+ * unit and from the transient buffers; units may share read-only gradients.
+ * Errors: as z3_step_layer for each unit, n_units < 1, n_full not in 1..8,
+ * gather_stream NULL or equal to stream when n_full >= 2, overlapping
+ * buffers (INVALID_ARG, naming the units). */
 z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16_t *const *full,
                         int32_t n_full, const z3_adam_hp *hp, int64_t step,
                         z3_stream stream, z3_stream gather_stream);
