@@ -47,8 +47,11 @@
  *     anything.
  *   - Output buffers must not overlap any other buffer of the same call
  *     (Z3_ERR_INVALID_ARG), except the in-place state of the Adam calls.
- *   - Calls make no synchronous CUDA calls and allocate nothing, so a caller
- *     may capture them in a CUDA graph.
+ *   - Calls make no synchronous CUDA calls and allocate no device memory, so
+ *     a caller may capture them in a CUDA graph.  The only CUDA objects the
+ *     library creates are events: per call in z3_model_step with prefetch
+ *     (destroyed before it returns), and once per pipeline in
+ *     z3_host_step_create.
  *   - A layout handle is immutable after creation and may be shared between
  *     threads.
  */
