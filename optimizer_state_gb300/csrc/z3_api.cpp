@@ -621,9 +621,13 @@ extern "C" z3_status z3_host_step_run(z3_host_step *p, const uint16_t *grads_hos
                                    v, shards, full, hp, step, &a);
     if (st != Z3_OK) return st;
     const int64_t T = L->psi_padded;
-    const Buf dev[2] = {{p->staging[1 - b], p->grad_bytes, "the other staging buffer"},
-                        {shards, 2 * T, "shards"}};
-    st = check_bufs(fn, dev, 2);
+    const Buf dev[6] = {{p->staging[1 - b], p->grad_bytes, "the other staging buffer"},
+                        {shards, 2 * T, "shards"},
+                        {master, 4 * T, "master"},
+                        {m, 4 * T, "m"},
+                        {v, 4 * T, "v"},
+                        {full, 2 * L->psi, "full"}};
+    st = check_bufs(fn, dev, 6);
     if (st != Z3_OK) return st;
     if (p->grad_bytes > 0 && grads_host == nullptr)
         return fail(Z3_ERR_INVALID_ARG, "z3_host_step_run: grads_host is NULL");
