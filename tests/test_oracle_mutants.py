@@ -61,6 +61,16 @@ MUTANTS = {
                 }"""),
     "reduce-scatter reads the next rank's slice": (
         "full_off[p] + i, scale);", "full_off[p] + (i + shard_numel[p] < numel[p] ? i + shard_numel[p] : i), scale);"),
+    "bf16 copy cast from the master before the update": (
+        "param_bf16[i] = or_bf16_from_f32(p1);", "param_bf16[i] = or_bf16_from_f32(p);"),
+    "partition starts the moments at the master": (
+        """                m[at] = 0.0f;
+                v[at] = 0.0f;""",
+        """                m[at] = x;
+                v[at] = x * x;"""),
+    "gather writes each rank's slice one element late": (
+        "memcpy(dst + (size_t)(full_off[p] + i) * elem,",
+        "memcpy(dst + (size_t)(full_off[p] + (i + 1 < numel[p] ? i + 1 : i)) * elem,"),
     "accumulate drops the running sum": (
         "out[at] = accumulate ? out[at] + g : g;", "out[at] = g;"),
     "eps inside the square root": (
