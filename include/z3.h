@@ -212,7 +212,10 @@ z3_status z3_step_layer(const z3_layout *layout, uint16_t *shards,
  * does not gather it forward or backward, and gathers it into `resident`
  * once, right after its update, so the copy always holds the current
  * parameters.  The caller fills `resident` once after z3_partition (one
- * z3_allgather). */
+ * z3_allgather).
+ *
+ * hp: NULL to use the step's hyperparameters, or this unit's own (a
+ * parameter group, e.g. no weight decay on norm gains). */
 typedef struct z3_unit {
     const z3_layout *layout;
     uint16_t *shards;
@@ -223,6 +226,7 @@ typedef struct z3_unit {
     int64_t grad_stride;
     float scale;
     uint16_t *resident;
+    const z3_adam_hp *hp;
 } z3_unit;
 
 /* One training step of a model of n_units units, in the schedule of [ZD]

@@ -364,8 +364,8 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
     for (int32_t i = 0; i < n_units; ++i) {
         const z3_unit &u = units[i];
         z3_status st = prepare_rs_adam(fn, u.layout, u.grads, u.grad_stride, u.scale, nullptr,
-                                       u.master, u.m, u.v, u.shards, u.resident, hp, step, &args[i],
-                                       "resident");
+                                       u.master, u.m, u.v, u.shards, u.resident,
+                                       u.hp != nullptr ? u.hp : hp, step, &args[i], "resident");
         if (st != Z3_OK) return st;
         const int64_t T = u.layout->psi_padded;
         int64_t gbytes = 0;

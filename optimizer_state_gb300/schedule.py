@@ -22,8 +22,10 @@ from . import z3
 class Unit:
     """Sharded state of one unit (a layer or the embedding)."""
 
-    def __init__(self, w: I.Workload, dev, gen: torch.Generator | None, grads: bool = True):
+    def __init__(self, w: I.Workload, dev, gen: torch.Generator | None, grads: bool = True,
+                 hp: dict | None = None):
         self.w = w
+        self.hp = hp                    # this unit's own hyperparameters (None: the step's)
         self.L = z3.Layout(w.numel, w.n_ranks)
         T = self.L.psi_padded
         self.shards = torch.empty(T, dtype=torch.bfloat16, device=dev)
@@ -91,12 +93,12 @@ class Model:
 
     def unit_args(self):
         return [(u.L, u.shards, u.master, u.m, u.v, u.grads, u.w.grad_stride,
-                 1.0 / u.w.n_ranks, u.resident) for u in self.units]
+                 1.0 / u.w.n_ranks, u.resident, u.hp) for u in self.units]
 
     @staticmethod
     def _update(u: Unit, hp: dict, t: int, stream):
         z3.z3_reduce_scatter_adam(u.L, u.grads, u.w.grad_stride, 1.0 / u.w.n_ranks, None,
-                                  u.master, u.m, u.v, u.shards, hp, t, stream=stream)
+                                  u.master, u.m, u.v, u.shards, u.hp or hp, t, stream=stream)
         if u.resident is not None:
             z3.z3_allgather(u.L, u.shards, u.resident, stream=stream)
 

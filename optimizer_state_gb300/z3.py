@@ -47,7 +47,8 @@ class Unit(ctypes.Structure):
     _fields_ = [("layout", ctypes.c_void_p), ("shards", ctypes.c_void_p),
                 ("master", ctypes.c_void_p), ("m", ctypes.c_void_p), ("v", ctypes.c_void_p),
                 ("grads", ctypes.c_void_p), ("grad_stride", ctypes.c_int64),
-                ("scale", ctypes.c_float), ("resident", ctypes.c_void_p)]
+                ("scale", ctypes.c_float), ("resident", ctypes.c_void_p),
+                ("hp", ctypes.POINTER(AdamHP))]
 
 
 class Traffic(ctypes.Structure):
@@ -295,21 +296,28 @@ def z3_reshard(src_layout: Layout, dst_layout: Layout, src, dst, stream=None):
 
 def z3_model_step(units, full, hp, step: int, stream=None, gather_stream=None):
     """units: sequence of (layout, shards, master, m, v, grads, grad_stride,
-    scale[, resident]) -- resident is None for a unit gathered at each use,
-    else that unit's persistent bf16 [Psi] copy; full: one transient buffer,
+    scale[, resident[, hp]]) -- resident is None for a unit gathered at each
+    use, else that unit's persistent bf16 [Psi] copy; hp is None for the
+    step's hyperparameters, else this unit's own; full: one transient buffer,
     or D + 1 of them for the prefetching schedule (then gather_stream is
     required)."""
     b16, f32 = _dtypes()
     arr = (Unit * len(units))()
+    own_hp = []                     # kept alive until the call returns
     need = 0
     for i, u in enumerate(units):
         L, sh, ma, m, v, g, stride, scale = u[:8]
         res = u[8] if len(u) > 8 else None
+        uhp = u[9] if len(u) > 9 else None
         T = L.psi_padded
+        hp_ptr = None
+        if uhp is not None:
+            own_hp.append(_hp(uhp))
+            hp_ptr = ctypes.pointer(own_hp[-1])
         arr[i] = Unit(L.handle.value, _dev(sh, b16, T, "shards"), _dev(ma, f32, T, "master"),
                       _dev(m, f32, T, "m"), _dev(v, f32, T, "v"),
                       _dev(g, b16, L.n_ranks * stride, "grads"), stride, scale,
-                      None if res is None else _dev(res, b16, L.psi, "resident"))
+                      None if res is None else _dev(res, b16, L.psi, "resident"), hp_ptr)
         if res is None:
             need = max(need, L.psi)
     fulls = (ctypes.c_void_p * len(full))(*[_dev(f, b16, need, "full") for f in full])

@@ -206,7 +206,10 @@ static int run_model(const char *in_path, const char *out_path, int32_t n_ranks,
     uint16_t *d_grads_all;
     CUDA_OK(cudaMalloc((void **)&d_full, sizeof(float) * (size_t)(psi > 0 ? psi : 1)));
     CUDA_OK(cudaMalloc((void **)&d_grads_all, sizeof(uint16_t) * (size_t)(n_ranks * stride + 8)));
-    CUDA_OK(cudaMemcpy(d_full, h_full, sizeof(float) * (size_t)psi, cudaMemcpyHostToDevice));
+    /* every copy goes on `stream`: the library's launches there (and on
+     * gstream, which the library orders after `stream`) see them complete */
+    CUDA_OK(cudaMemcpyAsync(d_full, h_full, sizeof(float) * (size_t)psi, cudaMemcpyHostToDevice,
+                            stream));
 
     z3_unit *units = calloc((size_t)n_params, sizeof(z3_unit));
     z3_layout **L = calloc((size_t)n_params, sizeof(z3_layout *));
@@ -232,8 +235,8 @@ static int run_model(const char *in_path, const char *out_path, int32_t n_ranks,
          * the full parameter vector to the start of its own allocation */
         float *d_unit = NULL;
         CUDA_OK(cudaMalloc((void **)&d_unit, sizeof(float) * (size_t)(numel[p] > 0 ? numel[p] : 1)));
-        CUDA_OK(cudaMemcpy(d_unit, d_full + off, sizeof(float) * (size_t)numel[p],
-                           cudaMemcpyDeviceToDevice));
+        CUDA_OK(cudaMemcpyAsync(d_unit, d_full + off, sizeof(float) * (size_t)numel[p],
+                                cudaMemcpyDeviceToDevice, stream));
         Z3_OK_OR_FAIL(z3_partition(L[p], d_unit, u->shards, u->master, u->m, u->v, stream));
         CUDA_OK(cudaStreamSynchronize(stream));
         cudaFree(d_unit);
@@ -257,14 +260,15 @@ static int run_model(const char *in_path, const char *out_path, int32_t n_ranks,
             return 1;
         }
         CUDA_OK(cudaStreamSynchronize(stream));   /* the last step no longer reads the grads */
-        CUDA_OK(cudaMemcpy(d_grads_all, h_grads, sizeof(uint16_t) * n, cudaMemcpyHostToDevice));
+        CUDA_OK(cudaMemcpyAsync(d_grads_all, h_grads, sizeof(uint16_t) * n, cudaMemcpyHostToDevice,
+                                stream));
         off = 0;
         for (int32_t p = 0; p < n_params; ++p) {    /* unit p's columns of every rank's row */
             if (numel[p] > 0)
-                CUDA_OK(cudaMemcpy2D(ugrads[p], sizeof(uint16_t) * (size_t)ustride[p],
-                                     d_grads_all + off, sizeof(uint16_t) * (size_t)stride,
-                                     sizeof(uint16_t) * (size_t)numel[p], (size_t)n_ranks,
-                                     cudaMemcpyDeviceToDevice));
+                CUDA_OK(cudaMemcpy2DAsync(ugrads[p], sizeof(uint16_t) * (size_t)ustride[p],
+                                          d_grads_all + off, sizeof(uint16_t) * (size_t)stride,
+                                          sizeof(uint16_t) * (size_t)numel[p], (size_t)n_ranks,
+                                          cudaMemcpyDeviceToDevice, stream));
             off += numel[p];
         }
         Z3_OK_OR_FAIL(z3_model_step(units, n_params, fulls, 2, &hp, t, stream, gstream));

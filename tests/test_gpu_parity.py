@@ -372,3 +372,32 @@ def test_model_step_fuzzed(z3mod, orc, N, specs, depth):
                 assert np.array_equal(u16(r.t)[:c.L.psi], orc.allgather(c.O, c.o["shards"]))
                 assert r.guards_intact()
         assert all(f.guards_intact() for f in fulls)
+
+
+@pytest.mark.parametrize("depth", [0, 1])
+def test_model_step_per_unit_hyperparameters(z3mod, orc, depth):
+    """Units with their own hyperparameters (a parameter group without weight
+    decay, one with another learning rate) next to units that use the
+    step's: every unit equals the oracle's layer step with its own
+    hyperparameters, bit for bit."""
+    N = 4
+    step_hp = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1)
+    own = [dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0), None,
+           dict(lr=3e-3, beta1=0.8, beta2=0.99, eps=1e-6, weight_decay=0.05), None]
+    specs = [[77, 1024], [100003, 7], [4099, 65536], [262147]]
+    cases = [Case(z3mod, orc, numel, N, seed=500 + i) for i, numel in enumerate(specs)]
+    big = max(c.L.psi for c in cases)
+    fulls = [Guarded(big, torch.bfloat16) for _ in range(depth + 1)]
+    gstream = torch.cuda.Stream() if depth else None
+    for t in (1, 2, 3):
+        drawn = [c.grads() for c in cases]
+        units = [(c.L, c.shards.t, c.master.t, c.m.t, c.v.t, g, c.stride, 1.0 / N, None, h)
+                 for c, (g, _), h in zip(cases, drawn, own)]
+        z3mod.z3_model_step(units, [f.t for f in fulls], step_hp, t, gather_stream=gstream)
+        for c, (_, gh), h in zip(cases, drawn, own):
+            orc.step_layer(c.O, c.o["shards"], gh, c.stride, 1.0 / N, c.o["master"], c.o["m"],
+                           c.o["v"], h or step_hp, t)
+        torch.cuda.synchronize()
+        for c in cases:
+            assert_adam_equal(c.device_state(), c.o)
+            assert c.guards_ok()
