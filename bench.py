@@ -633,8 +633,9 @@ def run_e2e(args, z3, L, w, rep, stream, sid, step_bytes, world):
     e1.record(stream)
     torch.cuda.synchronize()
     pipe.close()
-    ms = e0.elapsed_time(e1)
-    value = world * step_bytes * k / (ms * 1e-3) / 1e9
+    # the slowest rank's time: every rank runs this leg (world > 1 under torchrun)
+    ms = max_over_ranks(e0.elapsed_time(e1), world, stream.device)
+    value = aggregate_gbs(world, step_bytes, k, ms)
     # no step can finish faster than its upload: step bytes / (upload bytes / link rate)
     bound = world * step_bytes / (h2d / (link * 1e9)) / 1e9
     return {"value": round(value, 2), "unit": "GB/s",
