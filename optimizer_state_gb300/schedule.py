@@ -1,15 +1,20 @@
 """Multi-layer ZeRO-3 step: the schedule of "The ZeRO-3 Diagram Most People
 Remember Is Wrong", s.3 over a whole model.
 
-Forward: AllGather of every unit (layer or embedding) in order.  Backward:
-for every unit in reverse order, AllGather again, then the fused
-reduce-scatter + Adam of that unit ("ZeRO Stage 3: Parameter Partitioning":
-the backward pass traverses layers in reverse).  Every gather lands in ONE
-transient buffer sized for the largest unit (same page: the transient buffer
-is bounded by the largest single layer).
+Forward: AllGather of every unit (layer, bucket of layers or embedding) in
+order.  Backward: for every unit in reverse order, AllGather again, then the
+fused reduce-scatter + Adam of that unit ("ZeRO Stage 3: Parameter
+Partitioning": the backward pass traverses layers in reverse).  Every gather
+lands in one transient buffer sized for the largest unit (same page: the
+transient buffer is bounded by the largest single layer); with prefetch
+depth D there are D + 1 of them.  A resident unit (persistence threshold) is
+never gathered before use: its kept copy is refreshed after its update.
 
-Argument marshalling and launch ordering only; every step runs in the CUDA
-library through :mod:`optimizer_state_gb300.z3`.
+The library schedules the step itself (z3_model_step); the call-by-call form
+(``step(..., on_gather=hook)``) issues the same schedule from Python so that
+a caller can run its own work where a unit's compute would sit.  Argument
+marshalling and launch ordering only; every step runs in the CUDA library
+through :mod:`optimizer_state_gb300.z3`.
 """
 from __future__ import annotations
 
