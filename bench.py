@@ -11,10 +11,21 @@ element) per second, plus params/s and the fraction of the 8 TB/s HBM
 figure.  Every step works on one of several rotating replicas of the layer
 state whose total is far above the 129 MB L2, so each step starts cold.
 
+The line also carries: the roofline of the fused kernel (timed per launch in
+a second event-bracketed pass; DRAM traffic from the committed ncu summary
+while the kernel source is unchanged), the e2e rate through the C ABI from
+pinned host memory (z3_host_step_run, uploads and read-backs inside the
+timed region), sampled SM clocks, the launch count, and the single-threaded
+CPU oracle on a bounded sample.
+
 Arms:
   default            the CUDA library (inputs resident in HBM)
   --impl reference   the plain CPU oracle on the host cores, on a bounded
                      sample of the same workload (rank 0 only)
+Other workloads (--workload): the 7B-style and prime-length layers, every
+device call alone (kernels_<layer>), the 24-layer model step with buckets,
+prefetch and resident units, the stage-1/2 and plain-DP variants, and the
+prime-length sweep; --graph replays the timed steps as one CUDA graph.
 Under torchrun (N > 1) every rank runs an independent replica (weak
 scaling); the timed region is bracketed by a barrier and the max over ranks
 is taken.
