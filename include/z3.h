@@ -272,7 +272,9 @@ z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16_t *const *
  * [N][grad_stride] each, 16-byte aligned, not overlapping) and both streams;
  * the pipeline owns only its CUDA events (created here, destroyed by
  * z3_host_step_destroy).  A pipeline belongs to one layout and one calling
- * thread at a time.  Errors: NULL layout, staging buffer or stream, equal
+ * thread at a time.  Its calls order work through events that persist from
+ * one call to the next, so they are meant for eager use, not for capture in
+ * a CUDA graph.  Errors: NULL layout, staging buffer or stream, equal
  * streams, misaligned or overlapping staging buffers, grad_stride as for
  * z3_reduce_scatter (INVALID_ARG / ALIGNMENT); event creation failing
  * (CUDA). */
