@@ -392,6 +392,21 @@ def len_tabs(L, kind):
     return -(-n // 40)
 
 
+def parse_full_step(name: str):
+    """full_step_nd16[_prefetch[<D>]][_bucket<k>][_persist<T>] -> (prefetch
+    depth D (1 when the digits are omitted, 0 without _prefetch), layers per
+    bucket k (1), persistence threshold T (0))."""
+    m = re.fullmatch(r"full_step_nd16(_prefetch(\d*))?(_bucket(\d+))?(_persist(\d+))?", name)
+    if m is None:
+        raise SystemExit(f"unknown workload {name}")
+    depth = (int(m.group(2)) if m.group(2) else 1) if m.group(1) else 0
+    bucket = int(m.group(4)) if m.group(3) else 1
+    persist = int(m.group(6)) if m.group(5) else 0
+    if bucket < 1 or depth > 7:
+        raise SystemExit(f"{name}: buckets of >= 1 layer, prefetch depth <= 7")
+    return depth, bucket, persist
+
+
 def run_multi(args, world, rank, local):
     """Full step (24 layers + embedding, N_d = 16) or one sweep point
     (AG, AG, 4 micro-batches reduced and accumulated, Adam fused with the
@@ -409,14 +424,7 @@ def run_multi(args, world, rank, local):
     stream = torch.cuda.current_stream()
     sid = stream.cuda_stream
     if args.workload.startswith("full_step_nd16"):
-        # full_step_nd16[_prefetch[<D>]][_bucket<k>][_persist<T>]
-        m = re.fullmatch(r"full_step_nd16(_prefetch(\d*))?(_bucket(\d+))?(_persist(\d+))?",
-                         args.workload)
-        if m is None:
-            raise SystemExit(f"unknown workload {args.workload}")
-        depth = (int(m.group(2)) if m.group(2) else 1) if m.group(1) else 0
-        bucket = int(m.group(4)) if m.group(3) else 1
-        persist = int(m.group(6)) if m.group(5) else 0
+        depth, bucket, persist = parse_full_step(args.workload)
         model = schedule.full_step_model(dev, seed=rank, prefetch=depth, bucket_layers=bucket,
                                          persistence_threshold=persist)
         step_bytes, psi, launches = model.step_bytes, model.psi, model.launches_per_step()

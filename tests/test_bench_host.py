@@ -60,3 +60,16 @@ def test_reduce_kernel_name_follows_the_phases():
     assert bench.reduce_kernel_name(z3.Layout([3072 * 1024, 1024], 8)) == "k_reduce_aligned"
     assert bench.reduce_kernel_name(z3.Layout([100003, 7, 4099], 3)) == "k_reduce_shifted"
     assert bench.reduce_kernel_name(z3.Layout([262147], 8)) == "k_reduce_aligned"
+
+
+def test_full_step_workload_names():
+    import pytest
+    assert bench.parse_full_step("full_step_nd16") == (0, 1, 0)
+    assert bench.parse_full_step("full_step_nd16_prefetch") == (1, 1, 0)
+    assert bench.parse_full_step("full_step_nd16_prefetch2_bucket4") == (2, 4, 0)
+    assert bench.parse_full_step("full_step_nd16_bucket6_persist100000") == (0, 6, 100000)
+    assert bench.parse_full_step("full_step_nd16_prefetch3_bucket2_persist5") == (3, 2, 5)
+    for bad in ("full_step_nd8", "full_step_nd16_bucket0", "full_step_nd16_prefetch9",
+                "full_step_nd16_persist", "full_step_nd16_bucket4_prefetch2"):
+        with pytest.raises(SystemExit):
+            bench.parse_full_step(bad)
