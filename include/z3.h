@@ -37,7 +37,9 @@
  * Conventions:
  *   - Every call returns a z3_status; no call aborts, prints or traps, and
  *     no device code asserts.  z3_last_error() gives the message of the
- *     last failure on the calling thread.
+ *     last failure on the calling thread.  A failed host allocation inside
+ *     the library (layouts, launch tables, the model step's bookkeeping,
+ *     pipelines) returns Z3_ERR_HOST_MEMORY.
  *   - Device calls validate every argument on the host, then enqueue on the
  *     caller's stream and return; a launch failure returns Z3_ERR_CUDA.
  *     Errors during execution surface at the caller's next synchronisation.
@@ -70,7 +72,8 @@ typedef enum z3_status {
     Z3_ERR_INVALID_ARG = 1, /* null/negative/inconsistent argument */
     Z3_ERR_ALIGNMENT = 2,   /* buffer not 16-byte aligned, bad grad_stride */
     Z3_ERR_OVERFLOW = 3,    /* a size does not fit int64 / the launch grid */
-    Z3_ERR_CUDA = 4         /* the CUDA runtime reported an error */
+    Z3_ERR_CUDA = 4,        /* the CUDA runtime reported an error */
+    Z3_ERR_HOST_MEMORY = 5  /* a host allocation of the library failed */
 } z3_status;
 
 /* Same type as cudaStream_t; NULL is the legacy default stream. */
@@ -81,7 +84,11 @@ typedef struct z3_layout z3_layout;
 
 /* Adam hyperparameters as real numbers.  Every constant of the update is
  * rounded once to binary32 on the host: beta1, 1-beta1, beta2, 1-beta2,
- * 1/(1-beta1^t), 1/(1-beta2^t), lr, eps and lr*weight_decay. */
+ * 1/(1-beta1^t), 1/(1-beta2^t), lr, eps and lr*weight_decay.  Accepted:
+ * finite values with 0 <= beta1, beta2 < 1, eps > 0, lr >= 0 and
+ * weight_decay >= 0, whose constants are finite in binary32 and whose eps
+ * stays above 0 there (eps = 0 would turn a pad position's 0/0 into NaN);
+ * anything else is Z3_ERR_INVALID_ARG. */
 typedef struct z3_adam_hp {
     double lr;
     double beta1;
@@ -191,12 +198,18 @@ z3_status z3_reduce_scatter_adam(const z3_layout *layout,
 
 /* One layer step in the order of [ZD] s.3: forward AllGather into full,
  * backward AllGather into full again, then the fused ReduceScatter + Adam
- * that rewrites the shards.  Three kernel launches on the stream. */
+ * that rewrites the shards.  Three kernel launches on the stream.
+ * grad_shards_or_NULL: NULL keeps the reduced gradient in registers (no
+ * fp32 gradient reaches memory).  Non-NULL (fp32 [N][S], written) also
+ * stores each rank's reduced gradient slice there, exactly as
+ * z3_reduce_scatter would write it (pad 0): the one-slice gradient buffer
+ * of [ZS] "Stage 2 also partitions gradients", for a caller that needs the
+ * gradient itself.  Same fused pass, 4 more bytes written per element. */
 z3_status z3_step_layer(const z3_layout *layout, uint16_t *shards,
                         uint16_t *full, const uint16_t *grads,
                         int64_t grad_stride, float scale, float *master,
-                        float *m, float *v, const z3_adam_hp *hp,
-                        int64_t step, z3_stream stream);
+                        float *m, float *v, float *grad_shards_or_NULL,
+                        const z3_adam_hp *hp, int64_t step, z3_stream stream);
 
 /* ---- a whole model step --------------------------------------------- */
 

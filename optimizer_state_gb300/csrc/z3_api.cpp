@@ -62,6 +62,11 @@ z3_status check_grads(const char *fn, const z3_layout *L, int64_t grad_stride, i
     return Z3_OK;
 }
 
+// The binary32 constants of one Adam step.  Rejected: non-finite values,
+// beta1 or beta2 outside [0, 1) (at 1 a bias correction divides by zero),
+// eps <= 0 (a pad position, g = m = v = 0, would compute 0/0), negative lr or
+// weight decay, and any constant that is not finite in binary32 or an eps
+// that rounds to 0 there.
 z3_status adam_constants(const char *fn, const z3_adam_hp *hp, int64_t step, AdamK *k) {
     if (hp == nullptr) return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": hp is NULL");
     if (step < 1) return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": step < 1");
@@ -69,6 +74,11 @@ z3_status adam_constants(const char *fn, const z3_adam_hp *hp, int64_t step, Ada
     for (double x : vals)
         if (!std::isfinite(x))
             return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": non-finite hyperparameter");
+    if (!(hp->beta1 >= 0.0 && hp->beta1 < 1.0) || !(hp->beta2 >= 0.0 && hp->beta2 < 1.0))
+        return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": beta1 and beta2 must lie in [0, 1)");
+    if (!(hp->eps > 0.0)) return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": eps must be > 0");
+    if (hp->lr < 0.0 || hp->weight_decay < 0.0)
+        return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": lr and weight_decay must be >= 0");
     k->b1 = (float)hp->beta1;
     k->c1 = (float)(1.0 - hp->beta1);
     k->b2 = (float)hp->beta2;
@@ -78,6 +88,13 @@ z3_status adam_constants(const char *fn, const z3_adam_hp *hp, int64_t step, Ada
     k->lr = (float)hp->lr;
     k->eps = (float)hp->eps;
     k->lwd = (float)(hp->lr * hp->weight_decay);
+    const float consts[9] = {k->b1, k->c1, k->b2, k->c2, k->rb1, k->rb2, k->lr, k->eps, k->lwd};
+    for (float x : consts)
+        if (!std::isfinite(x))
+            return fail(Z3_ERR_INVALID_ARG,
+                        std::string(fn) + ": an Adam constant is not finite in binary32");
+    if (!(k->eps > 0.0f))
+        return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": eps rounds to 0 in binary32");
     return Z3_OK;
 }
 
@@ -195,7 +212,7 @@ z3_status prepare_rs_adam(const char *fn, const z3_layout *L, const uint16_t *gr
                           int64_t grad_stride, float scale, const float *grad_acc, float *master,
                           float *m, float *v, uint16_t *shards, const uint16_t *extra_full,
                           const z3_adam_hp *hp, int64_t step, ReduceArgs *a,
-                          const char *extra_name = "full") {
+                          const char *extra_name = "full", float *grad_out = nullptr) {
     if (L == nullptr) return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": layout is NULL");
     if (!std::isfinite(scale)) return fail(Z3_ERR_INVALID_ARG, std::string(fn) + ": scale");
     z3_status st = adam_constants(fn, hp, step, &a->k);
@@ -204,15 +221,17 @@ z3_status prepare_rs_adam(const char *fn, const z3_layout *L, const uint16_t *gr
     st = check_grads(fn, L, grad_stride, &gbytes);
     if (st != Z3_OK) return st;
     const int64_t T = L->psi_padded;
-    const Buf bufs[7] = {{grads, L->psi ? gbytes : 0, "grads"},
+    const Buf bufs[8] = {{grads, L->psi ? gbytes : 0, "grads"},
                          {master, 4 * T, "master"},
                          {m, 4 * T, "m"},
                          {v, 4 * T, "v"},
                          {shards, 2 * T, "shards"},
                          {grad_acc, grad_acc ? 4 * T : 0, "grad_acc"},
-                         {extra_full, extra_full ? 2 * L->psi : 0, extra_name}};
-    st = check_bufs(fn, bufs, 7);
+                         {extra_full, extra_full ? 2 * L->psi : 0, extra_name},
+                         {grad_out, grad_out ? 4 * T : 0, "grad_shards"}};
+    st = check_bufs(fn, bufs, 8);
     if (st != Z3_OK) return st;
+    a->out = grad_out;
     a->grads = grads;
     a->stride = grad_stride;
     a->scale = scale;
@@ -226,7 +245,8 @@ z3_status prepare_rs_adam(const char *fn, const z3_layout *L, const uint16_t *gr
 // forward AllGather, backward AllGather, then ReduceScatter + Adam.  The
 // backward gather's predecessor (the forward gather) writes only `full`, so
 // it reads the shards early; the update's predecessor (the backward gather)
-// writes only `full`, so it reads gradients and state early.
+// writes only `full`, so it reads gradients and state early.  With a.out set
+// the update also stores the reduced gradient and runs plain.
 z3_status enqueue_step_layer(const char *fn, const z3_layout *L, const ReduceArgs &a,
                              uint16_t *shards, uint16_t *full, cudaStream_t s) {
     z3_status st;
@@ -241,7 +261,7 @@ z3_status enqueue_step_layer(const char *fn, const z3_layout *L, const ReduceArg
     }
     if (st != Z3_OK) return st;
     Range r3("z3/ReduceScatter+Adam");
-    return run_reduce(L, a, kRSAdam, s, fn, true);
+    return a.out ? run_reduce(L, a, kRSAdamOut, s, fn) : run_reduce(L, a, kRSAdam, s, fn, true);
 }
 }  // namespace
 
@@ -262,12 +282,12 @@ extern "C" z3_status z3_reduce_scatter_adam(const z3_layout *L, const uint16_t *
 
 extern "C" z3_status z3_step_layer(const z3_layout *L, uint16_t *shards, uint16_t *full,
                                    const uint16_t *grads, int64_t grad_stride, float scale,
-                                   float *master, float *m, float *v, const z3_adam_hp *hp,
-                                   int64_t step, z3_stream stream) {
+                                   float *master, float *m, float *v, float *grad_shards,
+                                   const z3_adam_hp *hp, int64_t step, z3_stream stream) {
     const char *fn = "z3_step_layer";
     ReduceArgs a{};
     z3_status st = prepare_rs_adam(fn, L, grads, grad_stride, scale, nullptr, master, m, v,
-                                   shards, full, hp, step, &a);
+                                   shards, full, hp, step, &a, "full", grad_shards);
     if (st != Z3_OK) return st;
     if (L->psi_padded == 0) return Z3_OK;
     Range range("z3/step_layer");
@@ -342,9 +362,13 @@ struct Events {
 };
 }  // namespace
 
-extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16_t *const *full,
-                                   int32_t n_full, const z3_adam_hp *hp, int64_t step,
-                                   z3_stream stream, z3_stream gather_stream) {
+namespace {
+// The body of z3_model_step.  Every host allocation happens before the
+// first launch, so a std::bad_alloc (thrown out of here) leaves nothing
+// enqueued.
+z3_status model_step(const z3_unit *units, int32_t n_units, uint16_t *const *full,
+                     int32_t n_full, const z3_adam_hp *hp, int64_t step, z3_stream stream,
+                     z3_stream gather_stream) {
     const char *fn = "z3_model_step";
     if (units == nullptr || n_units < 1)
         return fail(Z3_ERR_INVALID_ARG, "z3_model_step: no units");
@@ -441,6 +465,10 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
         }
     }
     const cudaStream_t s = (cudaStream_t)stream;
+    const int nb = n_full;
+    std::vector<bool> buffer_used((size_t)nb, false);
+    Events E;
+    E.ev.reserve((size_t)(2 + 2 * nb));
     Range range("z3/model_step");
     z3_status st = Z3_OK;
     // whether this call has enqueued a kernel on s (on g) yet: a launch may
@@ -489,8 +517,6 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
     // so their small grids reach the GPU first.
     // Events: 0 = entry, 1 = gathers done, 2.. = gathered[b], then freed[b].
     const cudaStream_t g = (cudaStream_t)gather_stream;
-    const int nb = n_full;
-    Events E;
     cudaError_t err = E.make(2 + 2 * nb);
     auto cuda_fail = [&](cudaError_t e) {
         return fail(Z3_ERR_CUDA, std::string(fn) + ": " + cudaGetErrorString(e));
@@ -507,7 +533,6 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
             ours_g = true;
         }
     }
-    std::vector<bool> buffer_used((size_t)nb, false);
     auto gather = [&](int32_t i) -> z3_status {
         const int b = i % nb;
         if (buffer_used[b]) {   // the unit that last used this buffer has been updated
@@ -539,6 +564,17 @@ extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16
     if ((err = cudaEventRecord(E.ev[1], g)) != cudaSuccess) return cuda_fail(err);
     if ((err = cudaStreamWaitEvent(s, E.ev[1], 0)) != cudaSuccess) return cuda_fail(err);
     return Z3_OK;
+}
+}  // namespace
+
+extern "C" z3_status z3_model_step(const z3_unit *units, int32_t n_units, uint16_t *const *full,
+                                   int32_t n_full, const z3_adam_hp *hp, int64_t step,
+                                   z3_stream stream, z3_stream gather_stream) {
+    try {
+        return model_step(units, n_units, full, n_full, hp, step, stream, gather_stream);
+    } catch (const std::bad_alloc &) {
+        return fail_host_memory("z3_model_step");
+    }
 }
 
 // --------------------------------------------------------------------------
@@ -585,7 +621,7 @@ extern "C" z3_status z3_host_step_create(const z3_layout *L, uint16_t *staging0,
     st = check_bufs(fn, bufs, 2);
     if (st != Z3_OK) return st;
     auto *p = new (std::nothrow) z3_host_step();
-    if (p == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_host_step_create: out of host memory");
+    if (p == nullptr) return fail_host_memory(fn);
     p->L = L;
     p->staging[0] = staging0;
     p->staging[1] = staging1;

@@ -63,5 +63,8 @@ namespace z3 {
 // Thread-local last-error message.
 z3_status fail(z3_status st, const std::string &msg);
 void clear_error();
+// Z3_ERR_HOST_MEMORY with the message "<fn>: out of host memory" (or no
+// message, if even that cannot be stored).  Allocates nothing that can throw.
+z3_status fail_host_memory(const char *fn) noexcept;
 
 }  // namespace z3

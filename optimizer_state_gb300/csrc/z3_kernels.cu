@@ -257,6 +257,7 @@ __device__ __forceinline__ void finish1(const ReduceArgs &a, int64_t x, float g,
         if constexpr (MODE == kRSAccAdam) {
             if (!pad) g = __fadd_rn(a.acc_in[x], g);
         }
+        if constexpr (MODE == kRSAdamOut) a.out[x] = g;
         float p = a.master[x], m = a.m[x], v = a.v[x];
         adam1(g, p, m, v, a.k);
         a.master[x] = p;
@@ -313,6 +314,7 @@ __device__ __forceinline__ void reduce_vector(const ReduceArgs &a, int n_ranks, 
         for (int l = 0; l < 8; ++l) g[l] = __fadd_rn(o[l], g[l]);
         st8f(a.out + x0, g);
     } else {
+        if constexpr (MODE == kRSAdamOut) st8f(a.out + x0, g);  // never EARLY: waited at entry
         float p[8], m[8], v[8];
         ld8f(a.master + x0, p);
         ld8f(a.m + x0, m);
@@ -698,7 +700,9 @@ cudaError_t launch_reduce(const z3_layout *L, const ReduceArgs &a, Mode mode,
                           cudaStream_t stream, bool early) {
     // Later tables of one call update disjoint shard ranges, so their
     // primary (this call's previous table) writes nothing they read; an
-    // unfused mode reads its own output buffer, so it never runs early.
+    // unfused mode reads its own output buffer, so it never runs early, and
+    // the fused mode that also stores the reduced gradient stays plain (its
+    // gradient store comes before the Adam arithmetic, ahead of any wait).
     bool first = true;
     for (const Tab &t : L->reduce_tabs) {
         const bool e = early || !first;
@@ -710,10 +714,11 @@ cudaError_t launch_reduce(const z3_layout *L, const ReduceArgs &a, Mode mode,
                 if (e) launch_reduce_tab<kRSAdam, true>(t, a, stream);
                 else launch_reduce_tab<kRSAdam, false>(t, a, stream);
                 break;
-            default:
+            case kRSAccAdam:
                 if (e) launch_reduce_tab<kRSAccAdam, true>(t, a, stream);
                 else launch_reduce_tab<kRSAccAdam, false>(t, a, stream);
                 break;
+            default: launch_reduce_tab<kRSAdamOut, false>(t, a, stream); break;
         }
     }
     return cudaGetLastError();

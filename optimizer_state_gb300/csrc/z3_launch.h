@@ -26,13 +26,14 @@ enum Mode : int {
     kRSAcc = 1,      // grad_shards = grad_shards + fold * scale
     kRSAdam = 2,     // Adam(fold * scale)
     kRSAccAdam = 3,  // Adam(grad_acc + fold * scale)
+    kRSAdamOut = 4,  // Adam(fold * scale), and fold * scale stored to grad_shards
 };
 
 struct ReduceArgs {
     const uint16_t *__restrict__ grads;  // [N][stride] bf16
     int64_t stride;
     float scale;
-    float *out;             // grad_shards (kRS, kRSAcc)
+    float *out;             // grad_shards (kRS, kRSAcc, kRSAdamOut)
     const float *acc_in;    // grad_acc (kRSAccAdam)
     float *master;
     float *m;
@@ -87,7 +88,8 @@ cudaError_t launch_partition(const z3_layout *L, const PartitionArgs &a, cudaStr
 // the library in the same call and writes nothing this launch reads (for
 // the gather: not the shards; for a fused reduce: not the gradients, running
 // sums, master, m or v).  The launch may then read before it waits for that
-// kernel (its stores still wait).  Ignored by the unfused reduce modes.
+// kernel (its stores still wait).  Ignored by the unfused reduce modes and
+// by kRSAdamOut.
 cudaError_t launch_allgather(const z3_layout *L, const uint16_t *shards, uint16_t *full,
                              cudaStream_t stream, bool early);
 cudaError_t launch_reduce(const z3_layout *L, const ReduceArgs &a, Mode mode,

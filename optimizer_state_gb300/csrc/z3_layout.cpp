@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <cstring>
 #include <limits>
+#include <memory>
 #include <new>
 
 #include "z3_internal.h"
@@ -95,8 +96,21 @@ z3_status build_tabs(z3_layout *L, bool gather, int64_t vec_per_tile, std::vecto
 }  // namespace
 
 z3_status fail(z3_status st, const std::string &msg) {
-    g_last_error = msg;
+    try {
+        g_last_error = msg;
+    } catch (const std::bad_alloc &) {
+        g_last_error.clear();
+    }
     return st;
+}
+
+z3_status fail_host_memory(const char *fn) noexcept {
+    try {
+        g_last_error = std::string(fn) + ": out of host memory";
+    } catch (...) {
+        g_last_error.clear();
+    }
+    return Z3_ERR_HOST_MEMORY;
 }
 
 void clear_error() { g_last_error.clear(); }
@@ -105,15 +119,13 @@ void clear_error() { g_last_error.clear(); }
 
 using namespace z3;
 
-extern "C" z3_status z3_layout_create(const int64_t *numel, int32_t n_params, int32_t n_ranks,
-                                      z3_layout **out) {
-    if (out == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_layout_create: out is NULL");
-    *out = nullptr;
-    if (numel == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_layout_create: numel is NULL");
-    if (n_params < 1) return fail(Z3_ERR_INVALID_ARG, "z3_layout_create: n_params < 1");
-    if (n_ranks < 1) return fail(Z3_ERR_INVALID_ARG, "z3_layout_create: n_ranks < 1");
-    z3_layout *L = new (std::nothrow) z3_layout();
-    if (L == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_layout_create: out of host memory");
+namespace {
+// The body of z3_layout_create (arguments checked).  A failed allocation
+// throws std::bad_alloc out of here; the partial layout is released first.
+z3_status layout_create(const int64_t *numel, int32_t n_params, int32_t n_ranks,
+                        z3_layout **out) {
+    std::unique_ptr<z3_layout> owner(new z3_layout());
+    z3_layout *L = owner.get();
     L->n_params = n_params;
     L->n_ranks = n_ranks;
     L->numel.resize(n_params);
@@ -123,26 +135,20 @@ extern "C" z3_status z3_layout_create(const int64_t *numel, int32_t n_params, in
     int64_t S = 0, psi = 0;
     for (int32_t p = 0; p < n_params; ++p) {
         const int64_t n = numel[p];
-        if (n < 0) {
-            delete L;
+        if (n < 0)
             return fail(Z3_ERR_INVALID_ARG, "z3_layout_create: numel[" + std::to_string(p) + "] < 0");
-        }
         const int64_t s = ceil_div(n, n_ranks);
         L->numel[p] = n;
         L->shard_numel[p] = s;
         L->shard_off[p] = S;
         L->full_off[p] = psi;
-        if (!add_ok(S, s, &S) || !add_ok(psi, n, &psi)) {
-            delete L;
+        if (!add_ok(S, s, &S) || !add_ok(psi, n, &psi))
             return fail(Z3_ERR_OVERFLOW, "z3_layout_create: element count overflows int64");
-        }
     }
     int64_t total, bytes;
     // every [N][S] buffer must be addressable in bytes at fp32 width
-    if (!mul_ok(S, n_ranks, &total) || !mul_ok(total, 4, &bytes) || !mul_ok(psi, 4, &bytes)) {
-        delete L;
+    if (!mul_ok(S, n_ranks, &total) || !mul_ok(total, 4, &bytes) || !mul_ok(psi, 4, &bytes))
         return fail(Z3_ERR_OVERFLOW, "z3_layout_create: N*S overflows int64");
-    }
     L->S = S;
     L->psi = psi;
     L->psi_padded = total;
@@ -150,13 +156,25 @@ extern "C" z3_status z3_layout_create(const int64_t *numel, int32_t n_params, in
                               &L->gather_tabs);
     if (st == Z3_OK)
         st = build_tabs(L, false, (int64_t)kReduceThreads * kReduceVecPerThread, &L->reduce_tabs);
-    if (st != Z3_OK) {
-        delete L;
-        return st;
-    }
-    *out = L;
+    if (st != Z3_OK) return st;
+    *out = owner.release();
     clear_error();
     return Z3_OK;
+}
+}  // namespace
+
+extern "C" z3_status z3_layout_create(const int64_t *numel, int32_t n_params, int32_t n_ranks,
+                                      z3_layout **out) {
+    if (out == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_layout_create: out is NULL");
+    *out = nullptr;
+    if (numel == nullptr) return fail(Z3_ERR_INVALID_ARG, "z3_layout_create: numel is NULL");
+    if (n_params < 1) return fail(Z3_ERR_INVALID_ARG, "z3_layout_create: n_params < 1");
+    if (n_ranks < 1) return fail(Z3_ERR_INVALID_ARG, "z3_layout_create: n_ranks < 1");
+    try {
+        return layout_create(numel, n_params, n_ranks, out);
+    } catch (const std::bad_alloc &) {
+        return fail_host_memory("z3_layout_create");
+    }
 }
 
 extern "C" void z3_layout_destroy(z3_layout *layout) { delete layout; }
@@ -215,6 +233,7 @@ extern "C" const char *z3_status_string(z3_status st) {
         case Z3_ERR_ALIGNMENT: return "Z3_ERR_ALIGNMENT";
         case Z3_ERR_OVERFLOW: return "Z3_ERR_OVERFLOW";
         case Z3_ERR_CUDA: return "Z3_ERR_CUDA";
+        case Z3_ERR_HOST_MEMORY: return "Z3_ERR_HOST_MEMORY";
     }
     return "Z3_ERR_UNKNOWN";
 }

@@ -19,7 +19,8 @@ from . import build as _build
 _lock = threading.Lock()
 _lib = None
 
-Z3_OK, Z3_ERR_INVALID_ARG, Z3_ERR_ALIGNMENT, Z3_ERR_OVERFLOW, Z3_ERR_CUDA = range(5)
+(Z3_OK, Z3_ERR_INVALID_ARG, Z3_ERR_ALIGNMENT, Z3_ERR_OVERFLOW, Z3_ERR_CUDA,
+ Z3_ERR_HOST_MEMORY) = range(6)
 
 # Every symbol include/z3.h declares.
 EXPORTS = ("z3_layout_create", "z3_layout_destroy", "z3_layout_info", "z3_layout_params",
@@ -91,7 +92,7 @@ def load():
             "z3_reduce_scatter": (st, [vp, vp, i64, vp, f32, i32, vp]),
             "z3_adam_shard_step": (st, [vp, vp, vp, vp, vp, vp, hp, i64, vp]),
             "z3_reduce_scatter_adam": (st, [vp, vp, i64, f32, vp, vp, vp, vp, vp, hp, i64, vp]),
-            "z3_step_layer": (st, [vp, vp, vp, vp, i64, f32, vp, vp, vp, hp, i64, vp]),
+            "z3_step_layer": (st, [vp, vp, vp, vp, i64, f32, vp, vp, vp, vp, hp, i64, vp]),
             "z3_allreduce": (st, [vp, vp, i64, vp, f32, vp]),
             "z3_scatter": (st, [vp, vp, vp, vp]),
             "z3_reshard": (st, [vp, vp, i32, vp, vp, vp]),
@@ -140,13 +141,19 @@ def _stream(stream):
 
 
 def _dev(t, dtypes, numel: int, name: str):
-    """Device address of a tensor (or a raw int address)."""
+    """Device address of a tensor (or a raw int address).  A tensor must live
+    on the current device: the library launches there, and every kernel
+    treats its buffers as that device's own memory."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
     if not t.is_cuda:
         raise ValueError(f"{name}: must be a CUDA tensor")
+    import torch
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name}: on {t.device}, but the current device is "
+                         f"cuda:{torch.cuda.current_device()}")
     if t.dtype not in dtypes:
         raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
     if not t.is_contiguous():
@@ -258,7 +265,9 @@ def z3_reduce_scatter_adam(layout: Layout, grads, grad_stride: int, scale: float
 
 
 def z3_step_layer(layout: Layout, shards, full, grads, grad_stride: int, scale: float, master,
-                  m, v, hp, step: int, stream=None):
+                  m, v, hp, step: int, stream=None, grad_shards=None):
+    """grad_shards: None (the C call's grad_shards_or_NULL = NULL) or an fp32
+    [N*S] tensor that receives the reduced gradient slices."""
     b16, f32 = _dtypes()
     T = layout.psi_padded
     h = _hp(hp)
@@ -266,7 +275,7 @@ def z3_step_layer(layout: Layout, shards, full, grads, grad_stride: int, scale: 
         layout.handle, _dev(shards, b16, T, "shards"), _dev(full, b16, layout.psi, "full"),
         _dev(grads, b16, layout.n_ranks * grad_stride, "grads"), grad_stride, scale,
         _dev(master, f32, T, "master"), _dev(m, f32, T, "m"), _dev(v, f32, T, "v"),
-        ctypes.byref(h), step, _stream(stream)))
+        _dev(grad_shards, f32, T, "grad_shards"), ctypes.byref(h), step, _stream(stream)))
 
 
 def z3_allreduce(layout: Layout, grads, grad_stride: int, out, scale: float, stream=None):

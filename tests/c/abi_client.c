@@ -158,7 +158,7 @@ int main(int argc, char **argv) {
             }
             CUDA_OK(cudaMemcpyAsync(grads, h_grads, sizeof(uint16_t) * n, cudaMemcpyHostToDevice, stream));
             Z3_OK_OR_FAIL(z3_step_layer(L, shards, gathered, grads, stride, 1.0f / (float)n_ranks,
-                                        master, m, v, &hp, t, stream));
+                                        master, m, v, NULL, &hp, t, stream));
             CUDA_OK(cudaStreamSynchronize(stream));  /* h_grads is reused next step */
         }
     }

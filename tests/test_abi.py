@@ -1,7 +1,10 @@
 """C-ABI library on the CPU: it builds for sm_103a, loads, exports every
 symbol include/z3.h declares, and its host logic (layout, accounting,
 argument validation) agrees with the oracle.  No kernel is launched here:
-every device call below fails validation before reaching CUDA."""
+every device call below fails validation before reaching CUDA.  The tests
+that pass made-up device addresses are marked no_device and run in a child
+process that sees no CUDA device (tests/conftest.py), so a validation that
+let a call through would end in a launch error, never in a memory access."""
 import ctypes
 import os
 import re
@@ -82,6 +85,7 @@ def test_layout_errors(lib):
     lib.z3_layout_destroy(None)  # no-op
 
 
+@pytest.mark.no_device
 def test_device_call_validation_without_gpu(lib):
     """Host-side checks return before any CUDA call (fake device addresses)."""
     L = z3.Layout([35, 13, 12], 4)
@@ -112,14 +116,21 @@ def test_device_call_validation_without_gpu(lib):
     assert s == z3.Z3_ERR_INVALID_ARG
     s, msg = st(lib.z3_adam_shard_step(L.handle, *bufs, None, 1, None))
     assert s == z3.Z3_ERR_INVALID_ARG
-    s, msg = st(lib.z3_step_layer(None, *bufs[:2], A, 64, 0.25, *bufs[2:], ctypes.byref(hp),
-                                  1, None))
+    s, msg = st(lib.z3_step_layer(None, *bufs[:2], A, 64, 0.25, *bufs[2:], None,
+                                  ctypes.byref(hp), 1, None))
     assert s == z3.Z3_ERR_INVALID_ARG
+    s, msg = st(lib.z3_step_layer(L.handle, bufs[0], bufs[1], A + (1 << 27), 64, 0.25,
+                                  *bufs[2:], bufs[3] + 64, ctypes.byref(hp), 1, None))
+    assert s == z3.Z3_ERR_INVALID_ARG and "grad_shards" in msg and "overlaps" in msg
+    s, msg = st(lib.z3_step_layer(L.handle, bufs[0], bufs[1], A + (1 << 27), 64, 0.25,
+                                  *bufs[2:], far + 8, ctypes.byref(hp), 1, None))
+    assert s == z3.Z3_ERR_ALIGNMENT and "grad_shards" in msg
     s, msg = st(lib.z3_reduce_scatter_adam(L.handle, A, 64, 0.25, None, A, far, far + 4096,
                                            far + 8192, ctypes.byref(hp), 1, None))
     assert s == z3.Z3_ERR_INVALID_ARG and "overlaps" in msg
 
 
+@pytest.mark.no_device
 def test_zero_size_layer_is_a_noop(lib):
     L = z3.Layout([0, 0], 4)
     assert (L.S, L.psi, L.psi_padded) == (0, 0, 0)
@@ -142,6 +153,7 @@ def test_product_never_reaches_the_oracle():
             assert not back.search(open(os.path.join(ROOT, "oracle", f)).read()), f
 
 
+@pytest.mark.no_device
 def test_stage_and_reshard_entry_validation(lib):
     """z3_allreduce, z3_scatter and z3_reshard reject bad arguments on the
     host (fake device addresses; nothing reaches CUDA)."""
@@ -163,6 +175,7 @@ def test_stage_and_reshard_entry_validation(lib):
     assert lib.z3_reshard(L.handle, None, 4, A, far, None) == z3.Z3_ERR_INVALID_ARG
 
 
+@pytest.mark.no_device
 def test_model_step_validation_without_gpu(lib):
     """z3_model_step rejects bad unit lists, buffer counts, streams and
     overlapping or misaligned buffers (resident copies included) before it
@@ -209,6 +222,7 @@ def test_model_step_validation_without_gpu(lib):
     assert T == 64
 
 
+@pytest.mark.no_device
 def test_host_step_validation_without_gpu(lib):
     """z3_host_step_create rejects bad layouts, streams and staging buffers
     before it creates any CUDA object (fake addresses and stream handles)."""
@@ -246,6 +260,7 @@ def test_host_step_validation_without_gpu(lib):
     lib.z3_host_step_destroy(None)                           # a no-op
 
 
+@pytest.mark.no_device
 def test_model_step_checks_many_units_quickly(lib):
     """The cross-unit overlap check scales to thousands of units: 4000
     disjoint units plus one whose master overlaps the first unit's shards
@@ -269,3 +284,65 @@ def test_model_step_checks_many_units_quickly(lib):
     msg = z3.last_error()
     assert s == z3.Z3_ERR_INVALID_ARG and "unit 0" in msg and f"({n})" in msg, msg
     assert dt < 1.0, dt
+
+
+@pytest.mark.no_device
+def test_adam_hyperparameter_rules(lib):
+    """Hyperparameters that would turn the update into inf/NaN are rejected
+    on the host: beta1 or beta2 outside [0, 1), eps <= 0 (a pad position
+    would compute 0/0), negative lr or weight decay, and values whose binary32
+    constants overflow or whose eps rounds to 0.  Accepted ones pass the
+    checks and reach the launch, which fails here because the process sees
+    no device."""
+    L = z3.Layout([35, 13, 12], 4)
+    A = 1 << 32
+    bufs = [A + i * (1 << 24) for i in range(5)]
+    good = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+    bad = [dict(beta1=1.0), dict(beta2=1.0), dict(beta1=-0.1), dict(beta2=1.5), dict(eps=0.0),
+           dict(eps=-1e-8), dict(lr=-1e-3), dict(weight_decay=-0.1), dict(eps=1e-50),
+           dict(lr=1e300), dict(lr=1e200, weight_decay=1e200)]
+    for change in bad:
+        hp = z3.AdamHP(**{**good, **change})
+        s = lib.z3_adam_shard_step(L.handle, *bufs, ctypes.byref(hp), 1, None)
+        assert s == z3.Z3_ERR_INVALID_ARG, (change, z3.last_error())
+        s = lib.z3_reduce_scatter_adam(L.handle, A, 64, 0.25, None, *bufs[1:4], bufs[4] + 4096,
+                                       ctypes.byref(hp), 1, None)
+        assert s == z3.Z3_ERR_INVALID_ARG, (change, z3.last_error())
+    for change in ({}, dict(beta1=0.0, beta2=0.0), dict(weight_decay=0.1), dict(lr=0.0)):
+        hp = z3.AdamHP(**{**good, **change})
+        s = lib.z3_adam_shard_step(L.handle, *bufs, ctypes.byref(hp), 1, None)
+        assert s == z3.Z3_ERR_CUDA, (change, z3.last_error())
+
+
+_OOM_CHILD = r"""
+import ctypes, resource, sys
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+from optimizer_state_gb300 import z3
+lib = z3.load()
+n = 20_000_000                       # 160 MB of element counts; the layout needs 4x that
+numel = np.ones(n, dtype=np.int64)
+with open("/proc/self/statm") as f:
+    vm = int(f.read().split()[0]) * resource.getpagesize()
+resource.setrlimit(resource.RLIMIT_AS, (vm + (96 << 20), resource.RLIM_INFINITY))
+out = ctypes.c_void_p()
+st = lib.z3_layout_create(numel.ctypes.data_as(ctypes.c_void_p), n, 8, ctypes.byref(out))
+msg = z3.last_error()
+print(st, out.value, msg)
+sys.exit(0 if st == z3.Z3_ERR_HOST_MEMORY and out.value is None and "host memory" in msg
+         else 1)
+"""
+
+
+@pytest.mark.no_device
+def test_host_out_of_memory_status(lib):
+    """A host allocation that fails inside the library returns
+    Z3_ERR_HOST_MEMORY (not Z3_ERR_INVALID_ARG) and leaves no layout: a
+    child process caps its address space just above its current size and
+    asks for a layout of 20 million parameters."""
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "-c", _OOM_CHILD, ROOT], capture_output=True, text=True,
+                       timeout=120)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert lib.z3_status_string(z3.Z3_ERR_HOST_MEMORY) == b"Z3_ERR_HOST_MEMORY"

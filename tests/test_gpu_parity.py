@@ -202,6 +202,30 @@ def test_layer_d1024_full_check(z3mod, orc):
     assert c.guards_ok()
 
 
+@pytest.mark.parametrize("numel,n_ranks", [([35, 13, 12], 4), ([100003, 7, 1, 0, 4099], 3),
+                                            ([65537, 33, 8191], 64), ([5, 3, 2], 8),
+                                            (list(I.LAYER_D1024.numel), 8)],
+                         ids=["tiny", "5p-N3", "3p-N64", "pad-only", "d1024"])
+def test_step_layer_writes_grad_shards(z3mod, orc, numel, n_ranks):
+    """z3_step_layer with grad_shards_or_NULL set: the reduced fp32 gradient
+    slices it stores equal the oracle's reduce-scatter output bit for bit
+    (pad 0), and the updated state equals the oracle's step as with NULL."""
+    c = Case(z3mod, orc, numel, n_ranks, seed=5)
+    gs = Guarded(c.L.psi_padded, torch.float32, fill=float("nan"))
+    c.bufs.append(gs)
+    for step in (1, 2, 3):
+        g, gh = c.grads()
+        z3mod.z3_step_layer(c.L, c.shards.t, c.gathered.t, g, c.stride, 1.0 / n_ranks,
+                            c.master.t, c.m.t, c.v.t, HP, step, grad_shards=gs.t)
+        _, fb, want_gs = orc.step_layer(c.O, c.o["shards"], gh, c.stride, 1.0 / n_ranks,
+                                        c.o["master"], c.o["m"], c.o["v"], HP, step)
+        got = c.device_state()
+        assert np.array_equal(bits32(f32(gs.t)), bits32(want_gs))
+        assert np.array_equal(u16(c.gathered.t), fb)
+        assert_adam_equal(got, c.o)
+    assert c.guards_ok()
+
+
 def test_weight_decay_and_other_hparams(z3mod, orc):
     hp = dict(lr=3e-4, beta1=0.8, beta2=0.95, eps=1e-6, weight_decay=0.1)
     c = Case(z3mod, orc, [4099, 77, 1024], 8, seed=3, grad_std=1.0)
