@@ -24,7 +24,8 @@
  * F_p = sum_{q<p} n_q; S = sum_p s_p; Psi = sum_p n_p.
  *
  * Buffers (all device memory, all owned by the caller; the library never
- * allocates or frees device memory):
+ * allocates or frees device memory -- its only device memory of its own is
+ * the static array described at z3_step_layer_noalloc):
  *   shards   bf16 [N][S]   rank r's shard at r*S; p's slice at r*S + o_p
  *   master, m, v, grad_shards   fp32 [N][S], same indexing
  *   full     bf16 [Psi]    one gathered copy of the layer, parameters
@@ -49,11 +50,11 @@
  *     anything.
  *   - Output buffers must not overlap any other buffer of the same call
  *     (Z3_ERR_INVALID_ARG), except the in-place state of the Adam calls.
- *   - Calls make no synchronous CUDA calls and allocate no device memory, so
- *     a caller may capture them in a CUDA graph.  The only CUDA objects the
- *     library creates are events: per call in z3_model_step with prefetch
- *     (destroyed before it returns), and once per pipeline in
- *     z3_host_step_create.
+ *   - Calls other than z3_step_layer_noalloc (see there) make no synchronous
+ *     CUDA calls and allocate no device memory, so a caller may capture them
+ *     in a CUDA graph.  The only CUDA objects the library creates are events:
+ *     per call in z3_model_step with prefetch (destroyed before it returns),
+ *     and once per pipeline in z3_host_step_create.
  *   - A layout handle is immutable after creation and may be shared between
  *     threads.
  */
@@ -349,6 +350,41 @@ z3_status z3_scatter(const z3_layout *layout, const float *full, float *shards,
 z3_status z3_reshard(const z3_layout *src_layout, const z3_layout *dst_layout,
                      int32_t elem_bytes, const void *src, void *dst,
                      z3_stream stream);
+
+/* ---- the layer step without a caller-supplied gather buffer ------------ */
+
+/* z3_step_layer for callers that cannot allocate device memory.  The pages
+ * that define the method have no counterpart of this call; it exists because
+ * some callers cannot call cudaMalloc (code running inside an allocator
+ * callback, a plugin that only receives buffers from its host framework, a
+ * process whose device memory is all reserved up front) and so cannot
+ * provide z3_step_layer's transient gather buffer `full`.
+ *
+ * The step is z3_step_layer's with grad_shards_or_NULL = NULL: the same
+ * kernels, the same results, and the caller still passes (and owns) shards,
+ * grads, master, m and v.  The two all-gathers write into a static array in
+ * the library's own device memory instead of `full`; nothing reads it back.
+ * Limits and sharing:
+ *   - The array holds 16,777,216 bf16 elements (32 MiB).  A layer with more
+ *     elements (Psi) is rejected with Z3_ERR_INVALID_ARG and a message that
+ *     names both sizes; nothing is enqueued.
+ *   - The array occupies 32 MiB on every GPU where the library's device code
+ *     is loaded, until the process exits.
+ *   - All calls on a device share it, and it keeps what the last call wrote.
+ *     Nothing in it needs to start at zero (each gather writes every element
+ *     the step uses), but calls that overlap on the GPU (on different streams,
+ *     without ordering between them) race on it.
+ *   - The first call on a device looks up the array's device address with
+ *     cudaGetSymbolAddress (with that device current) and keeps it.  Make that
+ *     first call before any stream capture.
+ * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine.  Errors: those of z3_step_layer, the size limit above, and
+ * Z3_ERR_CUDA if the address lookup fails. */
+z3_status z3_step_layer_noalloc(const z3_layout *layout, uint16_t *shards,
+                                const uint16_t *grads, int64_t grad_stride,
+                                float scale, float *master, float *m, float *v,
+                                const z3_adam_hp *hp, int64_t step,
+                                z3_stream stream);
 
 /* ---- errors ------------------------------------------------------------ */
 

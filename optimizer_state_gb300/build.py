@@ -25,7 +25,8 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-fmad=false", "-Xcompiler", "-f
               "-Xcompiler", "-Wall", f"-I{INCLUDE}"] + ARCH
 CXX_FLAGS = ["-O2", "-std=c++17", "-fPIC", "-Wall", "-Wextra", f"-I{INCLUDE}"]
 
-SOURCES = [("z3_layout.cpp", "cxx"), ("z3_api.cpp", "cxx"), ("z3_kernels.cu", "nvcc")]
+SOURCES = [("z3_layout.cpp", "cxx"), ("z3_api.cpp", "cxx"), ("z3_kernels.cu", "nvcc"),
+           ("z3_noalloc.cu", "nvcc")]
 HEADERS = ["z3_internal.h", "z3_launch.h"]
 
 

@@ -28,7 +28,7 @@ EXPORTS = ("z3_layout_create", "z3_layout_destroy", "z3_layout_info", "z3_layout
            "z3_adam_shard_step", "z3_reduce_scatter_adam", "z3_step_layer",
            "z3_allreduce", "z3_scatter", "z3_reshard", "z3_model_step",
            "z3_host_step_create", "z3_host_step_run", "z3_host_step_destroy",
-           "z3_status_string", "z3_last_error")
+           "z3_step_layer_noalloc", "z3_status_string", "z3_last_error")
 
 
 class Z3Error(RuntimeError):
@@ -101,6 +101,7 @@ def load():
             "z3_host_step_create": (st, [vp, vp, vp, i64, vp, vp, ctypes.POINTER(vp)]),
             "z3_host_step_run": (st, [vp, vp, vp, vp, f32, vp, vp, vp, hp, i64, vp, vp]),
             "z3_host_step_destroy": (None, [vp]),
+            "z3_step_layer_noalloc": (st, [vp, vp, vp, i64, f32, vp, vp, vp, hp, i64, vp]),
             "z3_status_string": (ctypes.c_char_p, [st]),
             "z3_last_error": (ctypes.c_size_t, [ctypes.c_char_p, ctypes.c_size_t]),
         }
@@ -276,6 +277,21 @@ def z3_step_layer(layout: Layout, shards, full, grads, grad_stride: int, scale: 
         _dev(grads, b16, layout.n_ranks * grad_stride, "grads"), grad_stride, scale,
         _dev(master, f32, T, "master"), _dev(m, f32, T, "m"), _dev(v, f32, T, "v"),
         _dev(grad_shards, f32, T, "grad_shards"), ctypes.byref(h), step, _stream(stream)))
+
+
+def z3_step_layer_noalloc(layout: Layout, shards, grads, grad_stride: int, scale: float, master,
+                          m, v, hp, step: int, stream=None):
+    """z3_step_layer whose gathers write into the library's own static
+    device array instead of a caller buffer: for callers that cannot
+    allocate device memory (at most 16,777,216 elements per layer)."""
+    b16, f32 = _dtypes()
+    T = layout.psi_padded
+    h = _hp(hp)
+    _check(load().z3_step_layer_noalloc(
+        layout.handle, _dev(shards, b16, T, "shards"),
+        _dev(grads, b16, layout.n_ranks * grad_stride, "grads"), grad_stride, scale,
+        _dev(master, f32, T, "master"), _dev(m, f32, T, "m"), _dev(v, f32, T, "v"),
+        ctypes.byref(h), step, _stream(stream)))
 
 
 def z3_allreduce(layout: Layout, grads, grad_stride: int, out, scale: float, stream=None):
