@@ -88,14 +88,17 @@ def measured_hbm_peak():
 
 
 def kernel_source_digest() -> str:
-    """Digest of the sources that decide what a kernel launch does: the
-    kernels and their launchers, their argument blocks, and the layout code
-    that builds the launch tables (not the C-ABI validation layer)."""
+    """Digest of what decides the code a kernel launch runs: the kernels and
+    their launchers, their argument blocks, the layout code that builds the
+    launch tables (not the C-ABI validation layer), and the compiler flags
+    the kernels are built with."""
     import hashlib
+    from optimizer_state_gb300 import build as libbuild
     h = hashlib.sha256()
     for name in ("z3_kernels.cu", "z3_launch.h", "z3_internal.h", "z3_layout.cpp"):
         with open(os.path.join(ROOT, "optimizer_state_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
+    h.update(repr((libbuild.NVCC_FLAGS, libbuild.ARCH)).encode())
     return h.hexdigest()[:16]
 
 
@@ -112,6 +115,26 @@ def profiled_traffic(kernel: str, workload: str):
     if not ent or ent.get("source_digest") != kernel_source_digest():
         return None
     return ent.get("dram_bytes_per_launch")
+
+
+def profiled_step_traffic(workload: str):
+    """DRAM bytes of one whole layer step (forward gather, backward gather,
+    fused update) from the committed ncu capture taken with caches left
+    alone, so that each kernel carries the write-backs its predecessor left
+    in L2; None unless that capture was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = rec.get("_per_step", {}).get(workload)
+    if not ent or ent.get("source_digest") != kernel_source_digest():
+        return None
+    return {"dram_bytes": ent["dram_bytes_per_step"],
+            "algorithmic_bytes": ent["algorithmic_bytes_per_step"],
+            "ratio": round(ent["dram_bytes_per_step"] / ent["algorithmic_bytes_per_step"], 4),
+            "capture": ent.get("capture")}
 
 
 class ClockSampler:
@@ -175,6 +198,25 @@ class ClockSampler:
                 "samples_inside_timed_region": len(inside)}
 
 
+class LeadIn:
+    """Device work enqueued just before a timed region's start event: it
+    writes a 512 MiB buffer (four times the 129 MB L2, so the region starts
+    with a cold cache) and keeps the GPU busy, about 80 us, while the host
+    enqueues the start event and the first launches.  Without it the region
+    would open on an idle GPU and count the host's first launch latency."""
+
+    NBYTES = 512 << 20
+
+    def __init__(self, dev):
+        import torch
+        self.buf = torch.empty(self.NBYTES, dtype=torch.uint8, device=dev)
+
+    def enqueue(self, stream):
+        import torch
+        with torch.cuda.stream(stream):
+            self.buf.zero_()
+
+
 # --------------------------------------------------------------------------
 # the CUDA arm
 # --------------------------------------------------------------------------
@@ -230,16 +272,22 @@ def run_cuda(args, world, rank, local):
         z3.z3_step_layer(L, rep.shards, rep.full, rep.grads, w.grad_stride, scale, rep.master,
                          rep.m, rep.v, HP, rep.step, stream=sid)
 
+    # the clock sampler starts before the warm-up, so that no idle gap
+    # precedes the timed region
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
     for i in range(args.warmup):
         step(reps[i % n_rep])
     torch.cuda.synchronize()
 
+    # The K timed steps (each with its own step counter) are captured once,
+    # through the same C-ABI calls, as one CUDA graph and replayed inside the
+    # timed region, unless --eager asks for stream launches (or the graph
+    # would hold more than 50,000 launches).
+    use_graph = not args.eager and launches_per_step * args.steps <= 50000
     graph = None
-    if args.graph:
-        # the K timed steps (each with its own step counter) captured once as
-        # one CUDA graph and replayed inside the timed region
-        if launches_per_step * args.steps > 50000:
-            raise SystemExit("--graph: too many launches in one graph; use fewer --steps")
+    if use_graph:
         cap = torch.cuda.Stream()
         cap.wait_stream(stream)
         graph = torch.cuda.CUDAGraph()
@@ -251,16 +299,15 @@ def run_cuda(args, world, rank, local):
                                  rep.master, rep.m, rep.v, HP, rep.step, stream=cap.cuda_stream)
         stream.wait_stream(cap)
         torch.cuda.synchronize()
+    lead = LeadIn(dev)
 
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
     # ---- timed region: K layer steps
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    lead.enqueue(stream)
     clocks.mark(True)
     e0.record(stream)
     if graph is not None:
@@ -276,10 +323,20 @@ def run_cuda(args, world, rank, local):
     ms_total = e0.elapsed_time(e1)
     clock_info = clocks.stop()
 
-    # ---- per-kernel timing pass (same launches, events between kernels)
-    kernel_steps = min(args.steps, args.kernel_steps)
+    # ---- per-kernel timing pass (same launches, events between kernels):
+    # one untimed iteration, then kernel_steps iterations behind a lead-in
+    kernel_steps = max(1, args.kernel_steps)
+
+    def kernel_iteration(rep):
+        rep.step += 1
+        z3.z3_allgather(L, rep.shards, rep.full, stream=sid)
+        z3.z3_allgather(L, rep.shards, rep.full, stream=sid)
+        z3.z3_reduce_scatter_adam(L, rep.grads, w.grad_stride, scale, None, rep.master, rep.m,
+                                  rep.v, rep.shards, HP, rep.step, stream=sid)
+    kernel_iteration(reps[0])
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(kernel_steps)]
     torch.cuda.synchronize()
+    lead.enqueue(stream)
     for i in range(kernel_steps):
         rep = reps[i % n_rep]
         rep.step += 1
@@ -321,17 +378,12 @@ def run_cuda(args, world, rank, local):
             "dtype": "f32",
             "data": "synthetic",
             "config": {
-                "workload": args.workload,
-                "layer": " ".join("x".join(map(str, sh)) for sh in w.shapes),
-                "psi": L.psi, "n_ranks": w.n_ranks, "S": L.S,
-                "storage": "bf16 params/grads, fp32 master/m/v",
-                "bytes_per_param": 2 * w.n_ranks + 34,
-                "step_bytes": step_bytes,
+                **layer_config(args.workload, w, L.psi, L.S),
                 "l2": f"{n_rep} rotating replicas of the layer state "
                       f"({n_rep * state_bytes / 1e9:.2f} GB > 129 MB L2), every step cold",
                 "parallelism": f"{world} independent replica(s), one per GPU",
-                "launch": (f"one CUDA graph of the {args.steps} timed steps" if args.graph
-                           else "stream launches"),
+                "launch": (f"one CUDA graph of the {args.steps} timed steps (captured through "
+                           f"z3_step_layer)" if use_graph else "stream launches"),
             },
             "params_per_s": round(world * L.psi * args.steps / (ms_max * 1e-3), 1),
             "pct_of_8tbs": round(100.0 * value / (NOMINAL_HBM_GBS * world), 2),
@@ -345,7 +397,10 @@ def run_cuda(args, world, rank, local):
                 "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
                 "traffic": traffic,
+                "traffic_scope": "one launch captured alone with caches flushed: a lower bound "
+                                 "(the write-backs a kernel leaves in L2 land in the next one)",
                 "algorithmic_bytes_per_launch": rs_bytes,
+                "traffic_per_step": profiled_step_traffic(args.workload),
             },
             "e2e": e2e,
             "gpu_launches": launches_per_step * args.steps,
@@ -377,13 +432,21 @@ def layer_workload(name: str):
 
 
 def reduce_kernel_name(L) -> str:
-    """The reduce kernel a layer's launch runs: the aligned one when every
-    (parameter, rank) chunk's full-space and shard-space indices agree modulo
-    the 8-element vector, else the window-shifting one."""
-    aligned = all((F + r * s - (r * L.S + o)) % 8 == 0
-                  for n, s, o, F in zip(L.numel, L.shard_numel, L.shard_off, L.full_off) if n
-                  for r in range(L.n_ranks))
-    return "k_reduce_aligned" if aligned else "k_reduce_shifted"
+    """The reduce kernel a layer's launches run.  The library launches once
+    per table of up to 40 non-empty parameters; a table runs the aligned
+    kernel when every (parameter, rank) chunk in it has equal full-space and
+    shard-space indices modulo the 8-element vector, else the
+    window-shifting one.  Tables that disagree give "mixed"."""
+    names = set()
+    params = [(s, o, F) for n, s, o, F in zip(L.numel, L.shard_numel, L.shard_off, L.full_off)
+              if n]
+    for t0 in range(0, len(params), 40):
+        aligned = all((F + r * s - (r * L.S + o)) % 8 == 0 for s, o, F in params[t0:t0 + 40]
+                      for r in range(L.n_ranks))
+        names.add("k_reduce_aligned" if aligned else "k_reduce_shifted")
+    if len(names) == 1:
+        return names.pop()
+    return "mixed: k_reduce_aligned and k_reduce_shifted"
 
 
 def len_tabs(L, kind):
@@ -496,6 +559,9 @@ def run_multi(args, world, rank, local):
                  "l2": f"{n_rep} rotating replicas"}
     else:
         raise SystemExit(f"unknown workload {args.workload}")
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
@@ -517,13 +583,12 @@ def run_multi(args, world, rank, local):
         stream.wait_stream(cap)
         torch.cuda.synchronize()
         extra["launch"] = f"one CUDA graph of the {args.steps} timed steps"
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
+    lead = LeadIn(dev)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    lead.enqueue(stream)
     clocks.mark(True)
     e0.record(stream)
     if graph is not None:
@@ -687,6 +752,24 @@ def host_link_h2d_gbs(host, dev_buf, stream, reps: int = 5) -> float:
 # the oracle on the host cores
 # --------------------------------------------------------------------------
 
+# Oracle calls timed per kernel, with their algorithmic bytes per unpadded
+# element (the GPU kernels' accounting).
+CPU_KERNELS = ("allgather", "reduce_scatter", "reduce_scatter_accumulate", "adam", "step_layer")
+
+
+def cpu_bytes_per_elem(kernel: str, n_ranks: int) -> int:
+    return {"allgather": 4, "reduce_scatter": 2 * n_ranks + 4,
+            "reduce_scatter_accumulate": 2 * n_ranks + 8, "adam": 30,
+            "step_layer": 2 * n_ranks + 34}[kernel]
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
 def oracle_sample(w, n_elems: int, seed: int):
     """A bounded sample of the workload for the CPU oracle: the first
     n_elems elements of the layer's parameter list as one layer (same N_d,
@@ -708,73 +791,194 @@ def oracle_sample(w, n_elems: int, seed: int):
     return sw, full, grads
 
 
-def time_oracle(w, n_elems, min_seconds, max_steps, warmup=1, seed=0):
-    import oracle
-    sw, full, grads = oracle_sample(w, n_elems, seed)
-    O = oracle.layout(sw.numel, sw.n_ranks)
-    sh, ma, m, v = oracle.partition(O, full)
-    t = 0
-    for i in range(warmup):
-        t += 1
-        oracle.step_layer(O, sh, grads, sw.grad_stride, 1.0 / sw.n_ranks, ma, m, v, HP, t)
-    steps = 0
-    t0 = time.perf_counter()
-    # exactly max_steps steps, or (with min_seconds > 0) until min_seconds pass
-    while steps < max_steps:
-        if min_seconds > 0 and steps > 0 and time.perf_counter() - t0 >= min_seconds:
-            break
-        t += 1
-        oracle.step_layer(O, sh, grads, sw.grad_stride, 1.0 / sw.n_ranks, ma, m, v, HP, t)
-        steps += 1
-    dt = time.perf_counter() - t0
-    step_bytes = (2 * sw.n_ranks + 34) * O.psi
-    return dict(gbs=step_bytes * steps / dt / 1e9, params_per_s=O.psi * steps / dt, steps=steps,
-                seconds=dt, psi=O.psi, ms_per_step=1e3 * dt / steps)
+class OraclePiece:
+    """One thread's share of an oracle run over a sample: the contiguous
+    range [a, b) of the sample's unpadded elements, as a one-parameter layer
+    over the same N_d with its own state and gradient buffers.  The oracle's
+    arithmetic is elementwise (plus the rank fold of each element), so a
+    piece's elements end up with exactly the values they get when the
+    oracle runs on the whole sample; only where they are stored differs."""
+
+    def __init__(self, orc, sw, full, grads, a: int, b: int):
+        import numpy as np
+        from optimizer_state_gb300 import inputs as I
+        n = b - a
+        self.a, self.b, self.n = a, b, n
+        self.O = orc.layout([n], sw.n_ranks)
+        self.stride = I.grad_stride(n)
+        self.grads = np.zeros(sw.n_ranks * self.stride, np.uint16)
+        for k in range(sw.n_ranks):
+            self.grads[k * self.stride:k * self.stride + n] = \
+                grads[k * sw.grad_stride + a:k * sw.grad_stride + b]
+        self.shards, self.master, self.m, self.v = orc.partition(
+            self.O, np.ascontiguousarray(full[a:b]))
+        self.gs = np.zeros(self.O.psi_padded, np.float32)
+        self.scale = 1.0 / sw.n_ranks
+
+    def run(self, orc, kernel: str, t: int):
+        """One call of `kernel` on this piece (t: the Adam step number)."""
+        if kernel == "allgather":
+            orc.allgather(self.O, self.shards)
+        elif kernel == "reduce_scatter":
+            orc.reduce_scatter(self.O, self.grads, self.stride, self.scale, out=self.gs)
+        elif kernel == "reduce_scatter_accumulate":
+            orc.reduce_scatter(self.O, self.grads, self.stride, self.scale, out=self.gs,
+                               accumulate=True)
+        elif kernel == "adam":
+            orc.adam(self.master, self.m, self.v, self.gs, self.shards, HP["lr"], HP["beta1"],
+                     HP["beta2"], HP["eps"], HP["weight_decay"], t)
+        elif kernel == "step_layer":
+            orc.step_layer(self.O, self.shards, self.grads, self.stride, self.scale, self.master,
+                           self.m, self.v, HP, t)
+        else:
+            raise ValueError(kernel)
+
+
+def split_sample(orc, sample, cores: int) -> list:
+    """The sample cut into min(cores, elements) near-equal contiguous pieces."""
+    sw, full, grads = sample
+    n = sw.psi
+    c = max(1, min(cores, n))
+    bounds = [n * i // c for i in range(c + 1)]
+    return [OraclePiece(orc, sw, full, grads, bounds[i], bounds[i + 1]) for i in range(c)]
+
+
+def run_pieces(orc, pieces, kernel: str, iters: int, t0: int) -> float:
+    """Every piece runs `iters` calls of `kernel` (Adam steps t0, t0+1, ...)
+    in its own thread; the oracle's C calls release the GIL.  Returns the
+    wall time from the common start to the last thread's end."""
+    if len(pieces) == 1:
+        start = time.perf_counter()
+        for i in range(iters):
+            pieces[0].run(orc, kernel, t0 + i)
+        return time.perf_counter() - start
+    barrier = threading.Barrier(len(pieces) + 1)
+    errors = []
+
+    def work(p):
+        barrier.wait()
+        try:
+            for i in range(iters):
+                p.run(orc, kernel, t0 + i)
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(e)
+    threads = [threading.Thread(target=work, args=(p,)) for p in pieces]
+    for th in threads:
+        th.start()
+    barrier.wait()
+    start = time.perf_counter()
+    for th in threads:
+        th.join()
+    dt = time.perf_counter() - start
+    if errors:
+        raise errors[0]
+    return dt
+
+
+def time_kernel(orc, pieces, kernel: str, n_ranks: int, seconds: float, t0: int) -> dict:
+    """One untimed call, then as many calls as fill about `seconds`."""
+    t1 = run_pieces(orc, pieces, kernel, 1, t0)
+    iters = max(1, min(10 ** 6, int(round(seconds / max(t1, 1e-6)))))
+    dt = run_pieces(orc, pieces, kernel, iters, t0 + 1)
+    n = sum(p.n for p in pieces)
+    return dict(gbs=cpu_bytes_per_elem(kernel, n_ranks) * n * iters / dt / 1e9,
+                params_per_s=n * iters / dt, iters=iters, seconds=dt, t_next=t0 + 1 + iters)
 
 
 def cpu_baseline(seconds: float) -> dict:
+    """The oracle, as it stands, on the full d=1024 layer: every kernel
+    single-threaded and split over all host cores (one contiguous piece of
+    the layer per thread), about seconds/10 each.  `value` is the layer step
+    on all cores."""
+    import oracle
     from optimizer_state_gb300 import inputs as I
+    oracle.build()
     w = I.LAYER_D1024
-    r = time_oracle(w, w.psi, min_seconds=seconds, max_steps=10 ** 6)
-    return {"value": round(r["gbs"], 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "params_per_s": round(r["params_per_s"], 1),
-            "sample": f"{r['steps']} full layer steps of layer_d1024_nd8 (Psi={r['psi']}) "
-                      f"in {r['seconds']:.1f} s, single-threaded C oracle"}
+    sample = oracle_sample(w, w.psi, seed=0)
+    cores = host_cores()
+    per_kernel = {}
+    modes = (("single", 1), ("all_cores", cores))
+    res = {}
+    for mode, c in modes:
+        pieces = split_sample(oracle, sample, c)
+        t = 1
+        for k in CPU_KERNELS:
+            share = 0.25 if k == "step_layer" else 0.1
+            r = time_kernel(oracle, pieces, k, w.n_ranks, seconds * share, t)
+            t = r["t_next"]
+            per_kernel.setdefault(k, {})[mode] = round(r["gbs"], 4)
+            res[(mode, k)] = r
+    step_all, step_one = res[("all_cores", "step_layer")], res[("single", "step_layer")]
+    return {"value": round(step_all["gbs"], 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "params_per_s": round(step_all["params_per_s"], 1),
+            "single": {"value": round(step_one["gbs"], 4), "cores": 1,
+                       "params_per_s": round(step_one["params_per_s"], 1)},
+            "per_kernel_gbs": per_kernel,
+            "sample": f"the full layer_d1024_nd8 layer (Psi={w.psi}); all_cores: {cores} threads, "
+                      f"each running the unchanged oracle on one contiguous piece of the layer "
+                      f"as its own one-parameter layer over N_d={w.n_ranks}; single: one thread; "
+                      f"about {seconds * 0.1:.1f} s per kernel and mode, "
+                      f"{seconds * 0.25:.1f} s for the layer step "
+                      f"({step_all['iters']} all-core and {step_one['iters']} single layer steps)"}
+
+
+def layer_config(name: str, w, L_psi: int, S: int) -> dict:
+    """The config keys that name a layer workload; both arms report them."""
+    return {"workload": name,
+            "layer": " ".join("x".join(map(str, sh)) for sh in w.shapes),
+            "psi": L_psi, "n_ranks": w.n_ranks, "S": S,
+            "storage": "bf16 params/grads, fp32 master/m/v",
+            "bytes_per_param": 2 * w.n_ranks + 34,
+            "step_bytes": (2 * w.n_ranks + 34) * L_psi}
 
 
 def run_reference(args, world, rank):
+    """The CPU oracle as the reference arm: each step is the layer step on a
+    bounded sample of the d=1024 layer (the whole layer when the budget
+    allows), split over all host cores as in cpu_baseline."""
     if rank != 0:
         return
+    import oracle
     from optimizer_state_gb300 import inputs as I
+    oracle.build()
     w = I.LAYER_D1024
+    cores = host_cores()
     # size the per-step sample so that warmup + steps fit the time budget
-    probe = time_oracle(w, 1 << 20, min_seconds=0.0, max_steps=1, warmup=0)
-    per_elem_s = probe["seconds"] / probe["psi"]
+    probe_n = 1 << 20
+    probe = split_sample(oracle, oracle_sample(w, probe_n, seed=1), cores)
+    per_elem_s = run_pieces(oracle, probe, "step_layer", 1, 1) / probe_n
     budget = args.reference_seconds / max(1, args.steps + args.warmup)
-    n = int(min(w.psi, max(w.n_ranks * 8, budget / per_elem_s)))
-    r = time_oracle(w, n, min_seconds=0.0, max_steps=args.steps, warmup=args.warmup)
+    n = int(min(w.psi, max(w.n_ranks * 8 * cores, budget / per_elem_s)))
+    pieces = split_sample(oracle, oracle_sample(w, n, seed=0), cores)
+    run_pieces(oracle, pieces, "step_layer", args.warmup, 1)
+    dt = run_pieces(oracle, pieces, "step_layer", args.steps, 1 + args.warmup)
+    gbs = (2 * w.n_ranks + 34) * n * args.steps / dt / 1e9
+    O = oracle.layout(w.numel, w.n_ranks)
+    config = layer_config("layer_d1024_nd8", w, O.psi, O.S)
+    config["sample_psi"] = n
     line = {
         "impl": "reference",
         "metric": METRIC,
-        "value": round(r["gbs"], 4),
+        "value": round(gbs, 4),
         "unit": "GB/s",
         "n_gpus": world,
-        "steps": r["steps"],
+        "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(r["ms_per_step"], 4),
+        "ms_per_step": round(1e3 * dt / args.steps, 4),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": "layer_d1024_nd8", "psi": w.psi, "n_ranks": w.n_ranks,
-                   "sample_psi": r["psi"]},
-        "params_per_s": round(r["params_per_s"], 1),
-        "cpu_baseline": {"value": round(r["gbs"], 4), "unit": "GB/s", "cores": 1,
+        "config": config,
+        "params_per_s": round(n * args.steps / dt, 1),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": len(pieces),
                          "kind": "oracle",
-                         "sample": f"each step: the first {r['psi']} elements of the layer "
-                                   f"as one layer over N_d={w.n_ranks}"},
-        "e2e": {"value": round(r["gbs"], 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                         "sample": f"each step: the first {n} elements of the layer, cut into "
+                                   f"{len(pieces)} contiguous pieces, each a one-parameter layer "
+                                   f"over N_d={w.n_ranks} run by the unchanged oracle in its own "
+                                   f"thread"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -790,7 +994,8 @@ def main():
                     help="layer_d1024_nd8 (default), layer_7b_nd8, layer_7b_nd64, "
                          "full_step_nd16[_prefetch[<D>]][_bucket<k>][_persist<T>], {dp,stage1,stage2}_d1024_nd8, "
                          "or sweep_n<N>_nd<R>")
-    ap.add_argument("--kernel-steps", type=int, default=500)
+    ap.add_argument("--kernel-steps", type=int, default=200,
+                    help="iterations of the per-kernel event pass (layer workloads)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cold-bytes", type=int, default=1536 << 20,
                     help="total bytes of rotating state replicas")
@@ -798,7 +1003,10 @@ def main():
     ap.add_argument("--reference-seconds", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--graph", action="store_true",
-                    help="full-step and sweep workloads: replay the timed steps as one CUDA graph")
+                    help="full-step, sweep and stage workloads: replay the timed steps as one "
+                         "CUDA graph (layer workloads always do, unless --eager)")
+    ap.add_argument("--eager", action="store_true",
+                    help="layer workloads: time stream launches instead of one CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
