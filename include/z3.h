@@ -375,8 +375,10 @@ z3_status z3_reshard(const z3_layout *src_layout, const z3_layout *dst_layout,
  *     the step uses), but calls that overlap on the GPU (on different streams,
  *     without ordering between them) race on it.
  *   - The first call on a device looks up the array's device address with
- *     cudaGetSymbolAddress (with that device current) and keeps it.  Make that
- *     first call before any stream capture.
+ *     cudaGetSymbolAddress (with that device current) and keeps it for the
+ *     rest of the process.  Make that first call before any stream capture,
+ *     and do not call this entry point on a device after cudaDeviceReset
+ *     there (the reset ends the context that the kept address belongs to).
  * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
  * routine.  Errors: those of z3_step_layer, the size limit above, and
  * Z3_ERR_CUDA if the address lookup fails. */
