@@ -45,3 +45,26 @@ def test_reference_arm_runs_on_rank_zero_only(capsys):
     args = argparse.Namespace(steps=3, warmup=3, reference_seconds=1.0)
     bench.run_reference(args, world=2, rank=1)
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_matches_the_gpu_config(capsys):
+    """Rank 0 prints one reference line whose config carries the GPU line's
+    workload keys with the same values (plus the sample size), so the two
+    arms name the same workload."""
+    import argparse
+    import json
+
+    import bench
+    import oracle
+    from optimizer_state_gb300 import inputs as I
+    args = argparse.Namespace(steps=2, warmup=1, reference_seconds=0.6)
+    bench.run_reference(args, world=1, rank=0)
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    w = I.LAYER_D1024
+    O = oracle.layout(w.numel, w.n_ranks)
+    want = bench.layer_config("layer_d1024_nd8", w, O.psi, O.S)
+    assert {k: line["config"][k] for k in want} == want
+    assert 0 < line["config"]["sample_psi"] <= w.psi
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 1
+    assert line["cpu_baseline"]["cores"] >= 1 and line["value"] > 0
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
