@@ -240,16 +240,16 @@ def test_weight_decay_and_other_hparams(z3mod, orc):
 
 
 def test_rejects_bad_arguments_on_device(z3mod):
+    """Overlap is rejected with real buffers too (had the check slipped, the
+    gather would have stayed inside its own buffer).  Misaligned pointers are
+    checked in tests/test_abi.py, in a process that sees no device, since a
+    16-byte access at a misaligned address would fault."""
     L = z3mod.Layout([100, 28], 4)
     sh = torch.zeros(L.psi_padded, dtype=torch.bfloat16, device="cuda")
     full = torch.zeros(L.psi, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(z3mod.Z3Error) as e:
         z3mod.z3_allgather(L, sh, sh)          # in place: overlapping buffers
     assert e.value.status == z3mod.Z3_ERR_INVALID_ARG
-    big = torch.zeros(L.psi_padded + 8, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(z3mod.Z3Error) as e:
-        z3mod.z3_allgather(L, big[1:].data_ptr(), full)   # 2-byte offset: misaligned
-    assert e.value.status == z3mod.Z3_ERR_ALIGNMENT
     z3mod.z3_allgather(L, sh, full)
     torch.cuda.synchronize()
 
