@@ -98,7 +98,9 @@ def kernel_source_digest() -> str:
     for name in ("z3_kernels.cu", "z3_launch.h", "z3_internal.h", "z3_layout.cpp"):
         with open(os.path.join(ROOT, "optimizer_state_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
-    h.update(repr((libbuild.NVCC_FLAGS, libbuild.ARCH)).encode())
+    # include paths name where the repository sits, not what is compiled
+    flags = [f for f in libbuild.NVCC_FLAGS if not f.startswith("-I")]
+    h.update(repr((flags, libbuild.ARCH)).encode())
     return h.hexdigest()[:16]
 
 

@@ -54,6 +54,9 @@ def test_digest_covers_the_kernel_sources_and_flags(tmp_path, monkeypatch):
         assert (changed != base) == counted, name
     assert os.path.exists(os.path.join(csrc, "z3_api.cpp"))
     from optimizer_state_gb300 import build
+    moved = [f if not f.startswith("-I") else "-I/elsewhere/include" for f in build.NVCC_FLAGS]
+    monkeypatch.setattr(build, "NVCC_FLAGS", moved)
+    assert bench.kernel_source_digest() == base       # where the repository sits does not count
     monkeypatch.setattr(build, "NVCC_FLAGS", build.NVCC_FLAGS + ["-DSOMETHING"])
     assert bench.kernel_source_digest() != base
 
