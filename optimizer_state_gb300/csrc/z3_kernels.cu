@@ -114,16 +114,31 @@ struct TileRef {
     int64_t t;
 };
 
-__device__ __forceinline__ TileRef locate(const Tab &tab, int64_t g) {
+// The tiles of one launch number at most 2^31 - 1 (the layout starts a new
+// launch table before that), and every entry has at least one tile per
+// chunk, so the tile arithmetic fits unsigned 32 bits.  DIV32 divides by the
+// tiles per chunk in 32 bits instead of an emulated 64-bit division: the
+// copy kernels take it (their few instructions per element make the
+// division a large share); the reduce kernels keep the 64-bit form, with
+// which their fused modes fit 64 registers without spilling.
+template <bool DIV32>
+__device__ __forceinline__ TileRef locate(const Tab &tab, uint32_t g) {
     int lo = 0, hi = tab.count - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (tab.e[mid].tile0 <= g) lo = mid; else hi = mid - 1;
+        if ((uint32_t)tab.e[mid].tile0 <= g) lo = mid; else hi = mid - 1;
     }
-    const int64_t local = g - tab.e[lo].tile0;
-    const int64_t tpc = tab.e[lo].tpc;
-    const int64_t r = local / tpc;
-    return TileRef{lo, r, local - r * tpc};
+    if constexpr (DIV32) {
+        const uint32_t local = g - (uint32_t)tab.e[lo].tile0;
+        const uint32_t tpc = (uint32_t)tab.e[lo].tpc;
+        const uint32_t r = local / tpc;
+        return TileRef{lo, (int64_t)r, (int64_t)(local - r * tpc)};
+    } else {
+        const int64_t local = (int64_t)g - tab.e[lo].tile0;
+        const int64_t tpc = tab.e[lo].tpc;
+        const int64_t r = local / tpc;
+        return TileRef{lo, r, local - r * tpc};
+    }
 }
 
 // Programmatic dependent launch.  Every kernel is launched so that it may
@@ -199,7 +214,7 @@ template <bool ALIGNED, bool EARLY>
 __global__ void __launch_bounds__(kGatherThreads)
 k_allgather(const __grid_constant__ Tab tab, const GatherArgs a) {
     if constexpr (!EARLY) pdl_enter();
-    const TileRef tr = locate(tab, blockIdx.x);
+    const TileRef tr = locate<true>(tab, blockIdx.x);
     const TabEntry &e = tab.e[tr.p];
     const int64_t d0 = e.F + tr.r * e.s;
     const int64_t len = min(e.s, max((int64_t)0, e.n - tr.r * e.s));
@@ -381,7 +396,7 @@ k_reduce_aligned(const __grid_constant__ Tab tab, const ReduceArgs a) {
     static_assert(kReduceVecPerThread == 1, "one vector per thread");
     static_assert(!EARLY || MODE == kRSAdam || MODE == kRSAccAdam, "EARLY: fused modes only");
     if constexpr (!EARLY) pdl_enter();
-    const TileRef tr = locate(tab, blockIdx.x);
+    const TileRef tr = locate<false>(tab, blockIdx.x);
     const TabEntry &e = tab.e[tr.p];
     const int64_t c0 = tr.r * tab.S + e.o;
     const int64_t c_end = c0 + e.s;
@@ -404,7 +419,7 @@ __global__ void __launch_bounds__(kReduceThreads, 1024 / kReduceThreads)
 k_reduce_shifted(const __grid_constant__ Tab tab, const ReduceArgs a) {
     static_assert(!EARLY || MODE == kRSAdam || MODE == kRSAccAdam, "EARLY: fused modes only");
     if constexpr (!EARLY) pdl_enter();
-    const TileRef tr = locate(tab, blockIdx.x);
+    const TileRef tr = locate<false>(tab, blockIdx.x);
     const TabEntry &e = tab.e[tr.p];
     const int64_t c0 = tr.r * tab.S + e.o;
     const int64_t c_end = c0 + e.s;
@@ -437,7 +452,7 @@ k_reduce_shifted(const __grid_constant__ Tab tab, const ReduceArgs a) {
 __global__ void __launch_bounds__(kReduceThreads)
 k_partition(const __grid_constant__ Tab tab, const PartitionArgs a) {
     pdl_enter();
-    const TileRef tr = locate(tab, blockIdx.x);
+    const TileRef tr = locate<true>(tab, blockIdx.x);
     const TabEntry &e = tab.e[tr.p];
     const int64_t c0 = tr.r * tab.S + e.o;
     const int64_t c_end = c0 + e.s;
@@ -545,7 +560,7 @@ __global__ void __launch_bounds__(kFlatThreads, 4) k_allreduce(const AllreduceAr
 __global__ void __launch_bounds__(kReduceThreads) k_scatter(const __grid_constant__ Tab tab,
                                                             const ScatterArgs a) {
     pdl_enter();
-    const TileRef tr = locate(tab, blockIdx.x);
+    const TileRef tr = locate<true>(tab, blockIdx.x);
     const TabEntry &e = tab.e[tr.p];
     const int64_t c0 = tr.r * tab.S + e.o;
     const int64_t c_end = c0 + e.s;
@@ -592,7 +607,7 @@ k_reshard(const __grid_constant__ Tab tab, const __grid_constant__ SrcTab src_ta
           const T *__restrict__ src, T *__restrict__ dst) {
     static_assert(sizeof(T) == 2 || sizeof(T) == 4, "bf16 or fp32 words");
     pdl_enter();
-    const TileRef tr = locate(tab, blockIdx.x);
+    const TileRef tr = locate<true>(tab, blockIdx.x);
     const TabEntry &e = tab.e[tr.p];
     const int64_t s_src = src_tab.s[tr.p];
     const int64_t o_src = src_tab.o[tr.p];
