@@ -353,6 +353,19 @@ def run_cuda(args, world, rank, local):
     torch.cuda.synchronize()
     t_ag = sum(e[0].elapsed_time(e[1]) + e[1].elapsed_time(e[2]) for e in ev) / (2 * kernel_steps)
     t_rs = sum(e[2].elapsed_time(e[3]) for e in ev) / kernel_steps
+    # the gather back to back (kernel_steps calls between two events, rotating
+    # replicas): its launch latency overlaps the previous call's drain, as
+    # when a caller issues several gathers in a row
+    b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    lead.enqueue(stream)
+    b0.record(stream)
+    for i in range(kernel_steps):
+        rep = reps[i % n_rep]
+        z3.z3_allgather(L, rep.shards, rep.full, stream=sid)
+    b1.record(stream)
+    torch.cuda.synchronize()
+    t_ag_b2b = b0.elapsed_time(b1) / kernel_steps
 
     # ---- end to end through the public API with host buffers
     e2e = run_e2e(args, z3, L, w, reps[0], stream, sid, step_bytes, world)
@@ -389,7 +402,11 @@ def run_cuda(args, world, rank, local):
             },
             "params_per_s": round(world * L.psi * args.steps / (ms_max * 1e-3), 1),
             "pct_of_8tbs": round(100.0 * value / (NOMINAL_HBM_GBS * world), 2),
-            "kernels_ms": {"allgather": round(t_ag, 6), "reduce_scatter_adam": round(t_rs, 6)},
+            "kernels_ms": {"allgather": round(t_ag, 6), "reduce_scatter_adam": round(t_rs, 6),
+                           "allgather_back_to_back": round(t_ag_b2b, 6)},
+            "kernels_ms_how": "allgather and reduce_scatter_adam: each launch alone between two "
+                              "events (the roofline pass); allgather_back_to_back: consecutive "
+                              "calls between two events",
             "roofline": {
                 "kernel": f"{reduce_kernel_name(L)}<RSAdam> (fused reduce-scatter + Adam)",
                 "bound": "hbm",
