@@ -11,21 +11,28 @@ element) per second, plus params/s and the fraction of the 8 TB/s HBM
 figure.  Every step works on one of several rotating replicas of the layer
 state whose total is far above the 129 MB L2, so each step starts cold.
 
+Timed region: the clock sampler starts before the warm-up; the K timed steps
+are captured once (through z3_step_layer) as one CUDA graph and replayed
+(--eager: stream launches); a 512 MiB buffer write queued just before the
+start event leaves L2 cold and keeps the GPU busy while the host enqueues
+the region, so the region opens on queued work.
+
 The line also carries: the roofline of the fused kernel (timed per launch in
-a second event-bracketed pass; DRAM traffic from the committed ncu summary
-while the kernel source is unchanged), the e2e rate through the C ABI from
-pinned host memory (z3_host_step_run, uploads and read-backs inside the
-timed region), sampled SM clocks, the launch count, and the single-threaded
-CPU oracle on a bounded sample.
+a second event-bracketed pass; DRAM traffic per launch and per whole step
+from the committed ncu summaries while the kernel source is unchanged), the
+e2e rate through the C ABI from pinned host memory (z3_host_step_run,
+uploads and read-backs inside the timed region), sampled SM clocks, the
+launch count, and the CPU oracle on the full layer, every kernel on all host
+cores (one contiguous piece of the layer per thread) and on one.
 
 Arms:
   default            the CUDA library (inputs resident in HBM)
-  --impl reference   the plain CPU oracle on the host cores, on a bounded
+  --impl reference   the plain CPU oracle on all host cores, on a bounded
                      sample of the same workload (rank 0 only)
 Other workloads (--workload): the 7B-style and prime-length layers, every
 device call alone (kernels_<layer>), the 24-layer model step with buckets,
 prefetch and resident units, the stage-1/2 and plain-DP variants, and the
-prime-length sweep; --graph replays the timed steps as one CUDA graph.
+prime-length sweep; --graph replays their timed steps as one CUDA graph.
 Under torchrun (N > 1) every rank runs an independent replica (weak
 scaling); the timed region is bracketed by a barrier and the max over ranks
 is taken.
