@@ -92,6 +92,8 @@ def test_noalloc_step_matches_step_layer(z3mod, workload):
 
 @pytest.mark.no_device
 def test_noalloc_refuses_a_layer_beyond_its_scratch():
+    """Host-side checks of the entry point: the size limit, and the empty
+    layer."""
     from optimizer_state_gb300 import build, z3
     build.build()
     lib = z3.load()
@@ -103,3 +105,7 @@ def test_noalloc_refuses_a_layer_beyond_its_scratch():
     msg = z3.last_error()
     assert st == z3.Z3_ERR_INVALID_ARG
     assert "16777217" in msg and "16777216" in msg, msg
+    # an empty layer is a no-op that needs neither the array nor a device
+    L0 = z3.Layout([0, 0], 4)
+    assert lib.z3_step_layer_noalloc(L0.handle, None, None, 8, 0.25, None, None, None,
+                                     ctypes.byref(hp), 1, None) == z3.Z3_OK
