@@ -63,9 +63,10 @@ class Probe:
             g[self.valid] = (acc[self.valid] + g[self.valid]).astype(np.float32)
         p, m, v = self.master.copy(), self.m.copy(), self.v.copy()
         bf = np.zeros(self.xs.size, np.uint16)
+        grad = g.copy()
         orc.adam(p, m, v, g, bf, hp["lr"], hp["beta1"], hp["beta2"], hp["eps"],
                  hp["weight_decay"], t)
-        return dict(master=p, m=m, v=v, shards=bf)
+        return dict(master=p, m=m, v=v, shards=bf, grad=grad)
 
     def check_after(self, want, shards, master, m, v):
         got = dict(shards=u16(pick(shards, self.xs)), master=f32(pick(master, self.xs)),
@@ -101,12 +102,16 @@ def _layer_step(z3mod, orc, w, seed):
         grads = I.draw_grads(w, gen, dev)
         pr = Probe(orc, O, shards, master, m, v, seed=t)
         want = pr.expected(orc, grads, w.grad_stride, 1.0 / w.n_ranks, w.hp, t)
+        # the second step also stores the reduced gradient (grad_shards_or_NULL)
+        gsh = torch.full((T,), float("nan"), dtype=torch.float32, device=dev) if t == 2 else None
         z3mod.z3_step_layer(L, shards, full, grads, w.grad_stride, 1.0 / w.n_ranks, master, m,
-                            v, w.hp, t)
+                            v, w.hp, t, grad_shards=gsh)
         torch.cuda.synchronize()
         pr.check_gather(full)
         pr.check_after(want, shards, master, m, v)
-        del grads
+        if gsh is not None:
+            assert np.array_equal(bits32(f32(pick(gsh, pr.xs))), bits32(want["grad"]))
+        del grads, gsh
 
 
 @pytest.mark.parametrize("n_ranks", [8, 64])
