@@ -131,16 +131,22 @@ def run_all_calls(z3, orc, numel, n_ranks, seed, steps=2):
                        c.o["v"], HP, 2 * step, grad_acc=acc)
         assert_adam_equal(c.device_state(), c.o)
         assert np.array_equal(bits32(f32(gs.t)), bits32(want)), "grad_acc must be read only"
-    # the layer step: AG fwd, AG bwd, fused RS + Adam
+    # the layer step: AG fwd, AG bwd, fused RS + Adam; the second one also
+    # stores the reduced gradient (grad_shards_or_NULL)
     for step in range(2 * steps + 1, 2 * steps + 3):
         g, gh = c.grads()
+        out = gs.t if step % 2 == 0 else None
+        if out is not None:
+            out.fill_(float("nan"))
         z3.z3_step_layer(c.L, c.shards.t, c.gathered.t, g, c.stride, scale, c.master.t, c.m.t,
-                         c.v.t, HP, step)
-        ff, fb, _ = orc.step_layer(c.O, c.o["shards"], gh, c.stride, scale, c.o["master"],
-                                   c.o["m"], c.o["v"], HP, step)
+                         c.v.t, HP, step, grad_shards=out)
+        ff, fb, want_gs = orc.step_layer(c.O, c.o["shards"], gh, c.stride, scale, c.o["master"],
+                                         c.o["m"], c.o["v"], HP, step)
         got = c.device_state()
         assert np.array_equal(u16(c.gathered.t), fb)
         assert_adam_equal(got, c.o)
+        if out is not None:
+            assert np.array_equal(bits32(f32(out)), bits32(want_gs))
     assert c.guards_ok()
     return c
 
