@@ -914,8 +914,9 @@ def time_kernel(orc, pieces, kernel: str, n_ranks: int, seconds: float, t0: int)
 def cpu_baseline(seconds: float) -> dict:
     """The oracle, as it stands, on the full d=1024 layer: every kernel
     single-threaded and split over all host cores (one contiguous piece of
-    the layer per thread), about seconds/10 each.  `value` is the layer step
-    on all cores."""
+    the layer per thread), about seconds/10 each and seconds/4 for the layer
+    step.  `value` is the layer step on all cores; `cores` the threads it
+    used."""
     import oracle
     from optimizer_state_gb300 import inputs as I
     oracle.build()
@@ -925,8 +926,10 @@ def cpu_baseline(seconds: float) -> dict:
     per_kernel = {}
     modes = (("single", 1), ("all_cores", cores))
     res = {}
+    threads = {}
     for mode, c in modes:
         pieces = split_sample(oracle, sample, c)
+        threads[mode] = len(pieces)
         t = 1
         for k in CPU_KERNELS:
             share = 0.25 if k == "step_layer" else 0.1
@@ -935,12 +938,14 @@ def cpu_baseline(seconds: float) -> dict:
             per_kernel.setdefault(k, {})[mode] = round(r["gbs"], 4)
             res[(mode, k)] = r
     step_all, step_one = res[("all_cores", "step_layer")], res[("single", "step_layer")]
-    return {"value": round(step_all["gbs"], 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+    return {"value": round(step_all["gbs"], 4), "unit": "GB/s", "cores": threads["all_cores"],
+            "kind": "oracle",
             "params_per_s": round(step_all["params_per_s"], 1),
             "single": {"value": round(step_one["gbs"], 4), "cores": 1,
                        "params_per_s": round(step_one["params_per_s"], 1)},
             "per_kernel_gbs": per_kernel,
-            "sample": f"the full layer_d1024_nd8 layer (Psi={w.psi}); all_cores: {cores} threads, "
+            "sample": f"the full layer_d1024_nd8 layer (Psi={w.psi}); all_cores: "
+                      f"{threads['all_cores']} threads, "
                       f"each running the unchanged oracle on one contiguous piece of the layer "
                       f"as its own one-parameter layer over N_d={w.n_ranks}; single: one thread; "
                       f"about {seconds * 0.1:.1f} s per kernel and mode, "
