@@ -663,12 +663,17 @@ def run_kernels(args, local):
     bufs = [dict(full=torch.empty(L.psi, dtype=torch.bfloat16, device=dev),
                  gs=torch.zeros(L.psi_padded, dtype=torch.float32, device=dev),
                  gf=torch.empty(L.psi, dtype=torch.float32, device=dev),
-                 rs=torch.empty(L2.psi_padded, dtype=torch.float32, device=dev))
-            for _ in reps]
+                 rs=torch.empty(L2.psi_padded, dtype=torch.float32, device=dev),
+                 p32=I.draw_master(w, I.make_generator(50 + i, dev), dev))
+            for i in range(len(reps))]
     st = L.stats()
     psi = L.psi
     sc = 1.0 / N
     calls = {
+        # the initial partition (once per run): reads 4 B of fp32, writes the
+        # bf16 shard and fp32 master, m, v (14 B) per element
+        "partition": (18 * psi, lambda u, b, t: z3.z3_partition(u.L, b["p32"], u.shards, u.master,
+                                                               u.m, u.v)),
         "allgather": (st["hbm_allgather"], lambda u, b, t: z3.z3_allgather(u.L, u.shards, b["full"])),
         "reduce_scatter": (st["hbm_reduce_scatter"], lambda u, b, t: z3.z3_reduce_scatter(
             u.L, u.grads, w.grad_stride, b["gs"], sc)),

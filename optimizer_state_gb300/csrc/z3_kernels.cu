@@ -449,6 +449,10 @@ k_reduce_shifted(const __grid_constant__ Tab tab, const ReduceArgs a) {
 // Partition (initialisation): shard space <- full fp32, pad 0, m = v = 0
 // --------------------------------------------------------------------------
 
+// One vector (8 elements) per thread of each reduce tile, like k_scatter:
+// when the whole vector is valid, 16-byte stores of master, m, v and the
+// bf16 shard (and 16-byte loads of the full tensor when the table's chunks
+// have phase 0); element by element at chunk edges and in the pad.
 __global__ void __launch_bounds__(kReduceThreads)
 k_partition(const __grid_constant__ Tab tab, const PartitionArgs a) {
     pdl_enter();
@@ -458,9 +462,31 @@ k_partition(const __grid_constant__ Tab tab, const PartitionArgs a) {
     const int64_t c_end = c0 + e.s;
     const int64_t valid_end = c0 + min(e.s, max((int64_t)0, e.n - tr.r * e.s));
     const int64_t delta = e.F + tr.r * e.s - c0;
-    const int64_t x_beg = (c0 / kVec + tr.t * (int64_t)(kReduceThreads * kReduceVecPerThread)) * kVec;
-    const int64_t x_end = min(c_end, x_beg + (int64_t)(kReduceThreads * kReduceVecPerThread) * kVec);
-    for (int64_t x = max(x_beg, c0) + threadIdx.x; x < x_end; x += kReduceThreads) {
+    const int64_t x0 = (c0 / kVec + tr.t * (int64_t)kReduceThreads + threadIdx.x) * kVec;
+    if (x0 >= c_end) return;
+    if (x0 >= c0 && x0 + kVec <= valid_end) {
+        float f[8];
+        if (tab.phase0) {
+            ld8f(a.full + x0 + delta, f);
+        } else {  // source 4-byte aligned only
+#pragma unroll
+            for (int l = 0; l < 8; ++l) f[l] = a.full[x0 + delta + l];
+        }
+        const float zero[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        st8f(a.master + x0, f);
+        st8f(a.m + x0, zero);
+        st8f(a.v + x0, zero);
+        uint4 b;
+        b.x = pack_bf16x2(f[0], f[1]);
+        b.y = pack_bf16x2(f[2], f[3]);
+        b.z = pack_bf16x2(f[4], f[5]);
+        b.w = pack_bf16x2(f[6], f[7]);
+        *reinterpret_cast<uint4 *>(a.shards + x0) = b;
+        return;
+    }
+    for (int l = 0; l < kVec; ++l) {
+        const int64_t x = x0 + l;
+        if (x < c0 || x >= c_end) continue;  // another chunk's element
         const float val = x < valid_end ? a.full[x + delta] : 0.0f;
         a.master[x] = val;
         a.m[x] = 0.0f;
@@ -618,8 +644,15 @@ k_reshard(const __grid_constant__ Tab tab, const __grid_constant__ SrcTab src_ta
     if (x0 >= c_end) return;
     if (x0 >= c0 && x0 + kVec <= valid_end) {
         const int64_t i0 = tr.r * e.s + (x0 - c0);   // padded index of the first element
-        int64_t r = i0 / s_src;
-        int64_t j = i0 - r * s_src;
+        int64_t r, j;
+        if (i0 <= 0xffffffffll && s_src <= 0xffffffffll) {  // 32-bit division when it fits
+            const uint32_t q = (uint32_t)i0 / (uint32_t)s_src;
+            r = q;
+            j = i0 - (int64_t)q * s_src;
+        } else {
+            r = i0 / s_src;
+            j = i0 - r * s_src;
+        }
         T v[8];
 #pragma unroll
         for (int l = 0; l < 8; ++l) {
