@@ -28,8 +28,26 @@ def test_traffic_record_is_current_for_every_entry():
 def test_traffic_is_withheld_when_the_kernels_change(monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_digest", lambda: "0" * 16)
     assert bench.profiled_traffic("k_reduce_rs_adam", "layer_d1024_nd8") is None
+    assert bench.profiled_step_traffic("layer_d1024_nd8") is None
     monkeypatch.undo()
     assert bench.profiled_traffic("k_reduce_rs_adam", "no_such_workload") is None
+    assert bench.profiled_step_traffic("no_such_workload") is None
+
+
+def test_step_traffic_record_is_current_and_consistent():
+    """The whole-step record: current digest, read + write = total, the
+    three kernels add up to it, and no more DRAM bytes than algorithmic."""
+    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))["_per_step"]
+    for workload, ent in rec.items():
+        assert ent["source_digest"] == bench.kernel_source_digest(), workload
+        assert ent["dram_bytes_per_step"] == (ent["dram_bytes_read_per_step"] +
+                                              ent["dram_bytes_write_per_step"])
+        parts = ent["per_kernel"].values()
+        assert abs(sum(p["read"] for p in parts) - ent["dram_bytes_read_per_step"]) <= 3
+        assert abs(sum(p["write"] for p in parts) - ent["dram_bytes_write_per_step"]) <= 3
+        assert 0.5 < ent["dram_bytes_per_step"] / ent["algorithmic_bytes_per_step"] <= 1.0
+        got = bench.profiled_step_traffic(workload)
+        assert got["dram_bytes"] == ent["dram_bytes_per_step"]
 
 
 def test_digest_covers_the_kernel_sources_and_flags(tmp_path, monkeypatch):
